@@ -1,0 +1,158 @@
+/*
+ * ptgq.h -- C ABI of the GB300 (sm_103a) per-token-group 8-bit quantization library.
+ *
+ * The operation (sglang PR #30924, "unify per_token_group_quant into one trait-driven
+ * JIT kernel", sections "Implementation breakdown" and "Key source snippets"
+ * (ref_fp8_ue8m0); sglang PR #27449, "JIT port of per_token_group_quant_8bit_v2",
+ * sections "Summary" and "Implementation notes"; vLLM PR #41326, "Blackwell
+ * register-resident packed group quantization kernel", sections "Implementation
+ * breakdown" and "Key source snippets"):
+ *
+ *   For every live token row and every contiguous group of G elements of that row
+ *     v_i   = x_i                          (or silu(gate_i) * up_i, fused prologue)
+ *     amax  = max(max_i |v_i|, eps)
+ *     s     = amax / FMAX                  FMAX = 448 (e4m3) or 127 (int8)
+ *     UE8M0 formats: e = biased_exponent(s) + (mantissa(s) != 0), scale = 2^(e-127)
+ *     FP32  format : scale = s
+ *     q_i   = saturate(round_to_nearest_even(v_i / scale))   to e4m3fn or int8
+ *   All arithmetic is IEEE binary32 with round-to-nearest-even; silu uses the
+ *   correctly rounded binary32 exponential.  Codes and scales are bit-identical to
+ *   that definition (the library is tested against an independent CPU oracle).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named x, out_q, out_s, masked_m are DEVICE pointers (cudaMalloc or a
+ *     torch CUDA tensor) on the current device.  The caller owns every buffer; the
+ *     library allocates nothing, never synchronises, never reads device memory on
+ *     the host, and launches at most one kernel per call on `stream`, so a call can
+ *     be captured in a CUDA graph.
+ *   - Errors are returned as negative status codes (below) before anything is
+ *     launched; nothing is written in that case.  No exception crosses the ABI.
+ *     PTGQ_ERR_CUDA reports a launch failure taken from cudaGetLastError().
+ *   - The kernel is launched with programmatic stream serialization (PDL): it may
+ *     start while the previous kernel on `stream` finishes, and waits for it
+ *     (griddepcontrol.wait) before touching memory.
+ */
+#ifndef PTGQ_H_
+#define PTGQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ptgq_stream_t; /* the same type as cudaStream_t */
+
+/* Element type of x. */
+typedef enum { PTGQ_BF16 = 0, PTGQ_FP16 = 1 } ptgq_in_dtype;
+/* Element type of out_q: FP8 E4M3 ("fn", max 448) or int8. */
+typedef enum { PTGQ_E4M3 = 0, PTGQ_INT8 = 1 } ptgq_out_dtype;
+/* Scale format:
+ *   PTGQ_SCALE_FP32          float s per group.
+ *   PTGQ_SCALE_UE8M0_PACKED  exponent byte e per group, four groups per int32 word, group
+ *                            g in byte g % 4 (bits 8*(g%4)); unused bytes of the last word
+ *                            are zero (vLLM PR #41326, test ..._packed_all_zero).
+ *   PTGQ_SCALE_UE8M0_FP32    the power-of-two scale 2^(e-127) stored as a float. */
+typedef enum {
+  PTGQ_SCALE_FP32 = 0,
+  PTGQ_SCALE_UE8M0_PACKED = 1,
+  PTGQ_SCALE_UE8M0_FP32 = 2
+} ptgq_scale_fmt;
+/* Scale layout, with ncol = ng (float formats) or ceil(ng/4) (packed), rows = the out_q row
+ * extent of one block and mn_pad = round_up(rows, 4):
+ *   PTGQ_ROW_MAJOR      element (row, col) at row * ncol + col           ([rows, ncol])
+ *   PTGQ_COL_MAJOR_TMA  element (row, col) at col * mn_pad + row         ([ncol, mn_pad]),
+ *                       the TMA-aligned column-major layout (vLLM PR #41326, test
+ *                       ..._packed_all_zero; sglang PR #35593, "Implementation breakdown"
+ *                       item 3). */
+typedef enum { PTGQ_ROW_MAJOR = 0, PTGQ_COL_MAJOR_TMA = 1 } ptgq_scale_layout;
+
+/* Status codes. */
+enum {
+  PTGQ_OK = 0,
+  PTGQ_ERR_NULL = -1,       /* a required pointer is NULL */
+  PTGQ_ERR_DTYPE = -2,      /* unknown input dtype */
+  PTGQ_ERR_OUT_DTYPE = -3,  /* unknown output dtype */
+  PTGQ_ERR_GROUP = -4,      /* group_size not in {16, 32, 64, 128} (sglang PR #27449, "Notes") */
+  PTGQ_ERR_HIDDEN = -5,     /* hidden <= 0 or hidden % group_size != 0 */
+  PTGQ_ERR_SHAPE = -6,      /* negative count, or flat tokens_pad in (0, num_tokens) */
+  PTGQ_ERR_ALIGN = -7,      /* x not 32-byte, out_q not 16-byte or out_s not 4-byte aligned */
+  PTGQ_ERR_SCALE_FMT = -8,  /* unknown scale format */
+  PTGQ_ERR_LAYOUT = -9,     /* unknown scale layout */
+  PTGQ_ERR_EPS = -10,       /* eps not finite or below PTGQ_EPS_MIN */
+  PTGQ_ERR_FLAG = -11,      /* fuse_silu not 0 or 1, or an unknown flag bit */
+  PTGQ_ERR_TOO_LARGE = -12, /* sizes overflow the 63-bit index space */
+  PTGQ_ERR_CUDA = -13       /* the kernel launch failed */
+};
+
+/* Smallest accepted eps.  Down to this floor the kernel's division by the scale is proven
+ * to give the same codes as IEEE division for every input. */
+#define PTGQ_EPS_MIN 1e-24f
+
+/*
+ * ptgq_quant -- per-token-group quantization, flat or masked (EP-MoE) scheduler.
+ *
+ *   x               input, row-major, element type `dtype`.
+ *                     flat   (masked_m == NULL): [num_tokens, H_in]
+ *                     masked (masked_m != NULL): [E, tokens_pad, H_in]
+ *                   H_in = hidden, or 2*hidden with fuse_silu (gate columns [0, hidden),
+ *                   up columns [hidden, 2*hidden); sglang PR #27449, "Validation").
+ *                   32-byte aligned.
+ *   num_tokens_or_E flat: number of token rows T.  masked: number of experts E.
+ *   tokens_pad      flat: row extent of out_q (>= T, or 0 meaning T); rows [T, tokens_pad)
+ *                   of out_q and the padded scale rows are zero-filled (vLLM PR #41326,
+ *                   "Implementation breakdown" item 4).
+ *                   masked: rows per expert in x, out_q and the scales.
+ *   hidden          output width H; a multiple of group_size.
+ *   group_size      G in {16, 32, 64, 128}.
+ *   out_q           codes, row-major [rows, hidden] (flat) or [E, tokens_pad, hidden]
+ *                   (masked), element type `out_dtype`.  16-byte aligned.
+ *   out_s           scales: format `scale_fmt`, layout `scale_layout`; in masked mode one
+ *                   block per expert, blocks back to back.  ptgq_scale_elems() gives the
+ *                   number of elements (floats or int32 words).  4-byte aligned.
+ *   fuse_silu       1: v = silu(gate) * up computed in binary32 before quantization.
+ *   masked_m        NULL (flat) or device int32[E]: live rows of expert e are
+ *                   [0, masked_m[e]) (values outside [0, tokens_pad] are clamped).  In
+ *                   masked mode nothing outside the live rows is read or written: padding
+ *                   rows keep the caller's contents (sglang PR #35593, "Key source
+ *                   snippets", test_masked_rows_and_k_tail).
+ *   eps             floor of amax; finite and >= PTGQ_EPS_MIN.
+ *   stream          CUDA stream of the launch.
+ * Returns PTGQ_OK or a negative status.
+ */
+int ptgq_quant(const void* x, int dtype, int64_t num_tokens_or_E, int64_t tokens_pad,
+               int64_t hidden, int group_size, void* out_q, int out_dtype, void* out_s,
+               int scale_fmt, int scale_layout, int fuse_silu, const int32_t* masked_m,
+               float eps, ptgq_stream_t stream);
+
+/* Flags of ptgq_quant_ex. */
+enum {
+  /* Launch without programmatic stream serialization (plain stream order). */
+  PTGQ_FLAG_NO_PDL = 1,
+  /* vLLM semantics for UE8M0 scales: s = max(s, 1e-10) before rounding up to a power of
+   * two (vLLM PR #41326, test ..._packed_all_zero docstring: an all-zero group then gets
+   * exponent byte 0x5E).  No effect on PTGQ_SCALE_FP32. */
+  PTGQ_FLAG_UE8M0_SCALE_FLOOR = 2
+};
+
+/* ptgq_quant with option flags (a bitwise OR of PTGQ_FLAG_*); flags == 0 is ptgq_quant. */
+int ptgq_quant_ex(const void* x, int dtype, int64_t num_tokens_or_E, int64_t tokens_pad,
+                  int64_t hidden, int group_size, void* out_q, int out_dtype, void* out_s,
+                  int scale_fmt, int scale_layout, int fuse_silu, const int32_t* masked_m,
+                  float eps, ptgq_stream_t stream, unsigned flags);
+
+/* Size helper: the number of scale elements (floats, or int32 words for the packed format)
+ * that out_s must hold for these arguments (masked != 0 selects the masked layout, where
+ * num_tokens_or_E is E).  Host-only; touches no device.  Returns a status code. */
+int ptgq_scale_elems(int64_t num_tokens_or_E, int64_t tokens_pad, int64_t hidden,
+                     int group_size, int scale_fmt, int scale_layout, int masked,
+                     int64_t* n_out);
+
+/* A static, human-readable description of a status code. */
+const char* ptgq_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTGQ_H_ */
