@@ -1,0 +1,462 @@
+#!/usr/bin/env python3
+"""Benchmark of per-token-group 8-bit quantization on GB300.
+
+One step = one ptgq_quant call over one batch of the benchmarked workload:
+flat bf16 x [4096, 7168] (N(0,1), 0.1% outliers x100, 1% all-zero groups), G = 128,
+e4m3 codes, UE8M0 exponents packed four per int32 in the TMA-aligned column-major layout.
+
+Prints one JSON line.  ``value`` is the achieved HBM throughput in GB/s (algorithmic bytes:
+input read + codes written + scale words written, per call, over the device time of the
+timed steps, summed over ranks).  Timing: W warm-up steps, then K steps replayed from a
+CUDA graph, bracketed by barrier + synchronize, timed with CUDA events on the launching
+stream; inputs rotate over four buffer sets (353 MB) so each call reads from HBM, not L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (test infrastructure, single-threaded C++) on a
+bounded sample of the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and µs/call, per_token_group_quant FP8 G=128"
+WORKLOAD = "flat bf16 x[4096,7168] N(0,1)+0.1% outliers x100+1% zero groups, G=128, e4m3, " \
+           "UE8M0 packed int32 col-major (mn padded to 4, pads zero-filled)"
+T, H, G = 4096, 7168, 128
+BUFFER_SETS = 4
+GRAPH_CALLS = 400                      # calls captured per CUDA graph (a multiple of BUFFER_SETS)
+KERNEL_SOURCES = ["ptgq_kernel.cuh", "ptgq_math.cuh", "ptgq_api.cu", "ptgq_internal.h",
+                  "ptgq_inst_bf16.cu", "silu_tables.inc"]
+
+
+def algorithmic_bytes(tokens: int = T, hidden: int = H, group: int = G) -> int:
+    ng = hidden // group
+    words = (ng + 3) // 4 * ((tokens + 3) // 4 * 4)
+    return tokens * hidden * 2 + tokens * hidden + words * 4
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "fp8_token_group_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha") != kernel_source_sha() or d.get("workload") != "flat_outliers":
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("PTGQ_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(bytes_per_step: int, steps: int, world: int, max_elapsed_s: float) -> float:
+    """Whole-job GB/s: every rank processed `steps` calls of `bytes_per_step`."""
+    return world * steps * bytes_per_step / max_elapsed_s / 1e9
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_rate(x_cpu, rows_per_step: int, steps: int, warmup: int):
+    """Seconds per sample and GB/s of the oracle on `rows_per_step` rows of the workload."""
+    import numpy as np
+    import oracle as O
+    from fp8_token_group_gb300 import synth
+    sub = x_cpu[:rows_per_step].contiguous()
+    bits = synth.bits_u16(sub)
+    q = np.empty(rows_per_step * H, np.uint8)
+    s = np.empty(O.scale_elems(rows_per_step, 0, H, G, O.FMT_UE8M0_PACKED, O.LAYOUT_COL, 0),
+                 np.uint32)
+    run = lambda: O.quant(bits, O.IN_BF16, rows_per_step, 0, H, G, q, O.OUT_E4M3, s,
+                          O.FMT_UE8M0_PACKED, O.LAYOUT_COL, 0, None, 1e-10)
+    for _ in range(warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run()
+    el = time.perf_counter() - t0
+    nbytes = algorithmic_bytes(rows_per_step) * steps
+    return el, nbytes / el / 1e9
+
+
+def cpu_baseline(x_cpu, budget_s: float = 10.0) -> dict:
+    import oracle as O
+    O.build()
+    rows = 64
+    el, _ = oracle_rate(x_cpu, rows, 1, 1)
+    reps = max(1, int(budget_s / max(el, 1e-6)))
+    el, gbs = oracle_rate(x_cpu, rows, reps, 0)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} rows x {H} of the benchmarked input, {reps} repetitions "
+                      f"({el:.1f} s), single-threaded C++ oracle"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from fp8_token_group_gb300 import synth
+    import oracle as O
+    O.build()
+    x = synth.flat_outliers()
+    # size each step so the whole run stays within about a minute
+    el1, _ = oracle_rate(x, 1, 2, 1)
+    per_row = el1 / 2
+    rows = int(max(1, min(T, 60.0 / max(args.steps + args.warmup, 1) / max(per_row, 1e-7))))
+    el, gbs = oracle_rate(x, rows, args.steps, args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} rows x {H} per step, single-threaded C++ oracle"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU timing
+
+def build_sets(x_cpu, device):
+    import torch
+    import fp8_token_group_gb300 as P
+    sets = []
+    for _ in range(BUFFER_SETS):
+        xd = x_cpu.to(device)
+        q, s = P.alloc_outputs(xd, G, scale_fmt=P.SCALE_UE8M0_PACKED,
+                               scale_layout=P.COL_MAJOR_TMA)
+        sets.append((xd, q, s))
+    return sets
+
+
+def call(P, st):
+    xd, q, s = st
+    P.quant(xd, q, s, G, scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
+
+
+def time_graph(P, sets, steps: int, warmup: int, world: int, sampler=None):
+    """Capture GRAPH_CALLS calls (rotating buffer sets) and replay; returns elapsed s for
+    `steps` calls (rounded up to whole graphs) and the number of calls made."""
+    import torch
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            call(P, sets[i % len(sets)])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(GRAPH_CALLS):
+            call(P, sets[i % len(sets)])
+    reps = max(1, -(-steps // GRAPH_CALLS))
+    wreps = max(1, -(-warmup // GRAPH_CALLS))
+    with torch.cuda.stream(stream):
+        for _ in range(wreps):
+            g.replay()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    return start.elapsed_time(end) / 1e3, reps * GRAPH_CALLS, clocks
+
+
+def time_e2e(P, x_cpu, steps: int, device):
+    """Public API with host buffers: per step H2D of x (pinned), quantize, D2H of q and s."""
+    import torch
+    xh = x_cpu.pin_memory()
+    xd = torch.empty_like(xh, device=device)
+    q, s = P.alloc_outputs(xd, G, scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
+    qh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    sh = torch.empty(s.shape, dtype=s.dtype).pin_memory()
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        P.quant(xd, q, s, G, scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
+        qh.copy_(q, non_blocking=True)
+        sh.copy_(s, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    el = start.elapsed_time(end) / 1e3
+    h2d = xh.numel() * xh.element_size()
+    d2h = qh.numel() * qh.element_size() + sh.numel() * sh.element_size()
+    return el, h2d, d2h
+
+
+def other_workloads(P, device, steps: int) -> dict:
+    """Device throughput of the other large workloads (context for the roofline; each is a
+    parity-tested configuration, not a bench line)."""
+    import torch
+    from fp8_token_group_gb300 import synth
+    out = {}
+
+    def measure(name, make, nbytes, nsets):
+        sets = [make() for _ in range(nsets)]
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            for i in range(6):
+                sets[i % nsets][0]()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(100):
+                sets[i % nsets][0]()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // 100)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * 100)
+        nb = nbytes(sets[0][1])
+        out[name] = {"us_per_call": round(us, 3), "bytes_per_call": nb,
+                     "gbs": round(nb / us / 1e3, 1)}
+
+    # Each buffer set has its own input copy, so the sets together exceed L2.
+    # fused silu, flat bf16 [8192, 2x2048] -> e4m3 [8192, 2048], fp32 column-major scales
+    xs_cpu = synth.silu_flat()
+
+    def mk_silu():
+        xs = xs_cpu.to(device)
+        q, s = P.alloc_outputs(xs, G, fuse_silu=True, scale_layout=P.COL_MAJOR_TMA)
+        return (lambda: P.quant(xs, q, s, G, fuse_silu=True, scale_layout=P.COL_MAJOR_TMA)), None
+    measure("silu_flat_8192x2x2048", mk_silu,
+            lambda _: 8192 * 4096 * 2 + 8192 * 2048 + 32 * 8192 * 4, 4)
+
+    # masked silu, bf16 [32, 384, 2x4096], UE8M0 packed column-major
+    xm_cpu, mm = synth.masked_silu()
+    mmd = mm.to(device)
+    live = int(mm.clamp(0, 384).sum())
+
+    def mk_masked():
+        xm = xm_cpu.to(device)
+        q, s = P.alloc_outputs(xm, G, fuse_silu=True, masked=True,
+                               scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
+        return (lambda: P.quant(xm, q, s, G, fuse_silu=True, masked_m=mmd,
+                                scale_fmt=P.SCALE_UE8M0_PACKED,
+                                scale_layout=P.COL_MAJOR_TMA)), None
+    measure(f"masked_silu_32x384x2x4096_live{live}", mk_masked,
+            lambda _: live * (4096 * 2 * 2 + 4096 + 8 * 4), 2)
+
+    # sweep corner: bf16 [32768, 7168], G=128, e4m3, fp32 row-major (input > L2)
+    xb_cpu = synth.normal((32768, 7168), torch.bfloat16, seed=1)
+
+    def mk_big():
+        xb = xb_cpu.to(device)
+        q, s = P.alloc_outputs(xb, G)
+        return (lambda: P.quant(xb, q, s, G)), None
+    measure("sweep_32768x7168_G128_e4m3", mk_big, lambda _: 32768 * 7168 * 3 + 32768 * 56 * 4, 1)
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import fp8_token_group_gb300 as P
+    from fp8_token_group_gb300 import synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    P.lib()
+    x = synth.flat_outliers()
+    sets = build_sets(x, device)
+    sampler = ClockSampler(local) if rank == 0 else None
+    elapsed, calls, clocks = time_graph(P, sets, args.steps, args.warmup, world, sampler)
+    max_el = reduce_max(elapsed, world, device)
+    bpc = algorithmic_bytes()
+    value = aggregate(bpc, calls, world, max_el)
+    us = max_el / calls * 1e6
+    peak, peak_kind = measured_peak()
+    achieved = bpc / (elapsed / calls) / 1e9      # this rank's launches, per launch
+
+    e2e_el, h2d, d2h = time_e2e(P, x, max(3, min(args.steps, 50)), device)
+    e2e_el = reduce_max(e2e_el, world, device)
+    e2e_steps = max(3, min(args.steps, 50))
+    others = other_workloads(P, device, 2000) if (rank == 0 and not args.no_extra) else {}
+    base = cpu_baseline(x) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": calls, "warmup": args.warmup, "ms_per_step": round(max_el / calls * 1e3, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": T * world, "hidden": H,
+                       "group_size": G, "input": "bf16", "output": "e4m3",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": f"{BUFFER_SETS} rotating buffer sets "
+                             f"({BUFFER_SETS * bpc / 1e6:.0f} MB > 129 MB L2)",
+                       "timing": f"CUDA graph of {GRAPH_CALLS} calls replayed, CUDA events"},
+            "us_per_call": round(us, 3),
+            "tokens_per_s": round(world * T * calls / max_el, 1),
+            "pct_of_peak": round(100 * achieved / peak, 2),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "traffic": recorded_traffic(),
+                         "algorithmic_bytes_per_launch": bpc},
+            "clocks": clocks,
+            "gpu_launches": calls,
+            "e2e": {"value": round(world * e2e_steps * bpc / e2e_el / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "pinned host x -> device, fp8_token_group_gb300.quant, codes and "
+                            "scales -> pinned host, per step"},
+            "cpu_baseline": base,
+            "other_workloads": others,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone runs it, other ranks exit without work
+        return run_reference(args, int(os.environ.get("WORLD_SIZE", "1")),
+                             int(os.environ.get("RANK", "0")))
+    world, rank, local = dist_setup(args.gpus)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

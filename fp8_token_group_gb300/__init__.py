@@ -1,0 +1,180 @@
+"""GB300 (sm_103a) per-token-group 8-bit activation quantization.
+
+A thin ctypes binding over ``libptgq.so`` (the C ABI in ``include/ptgq.h``).  PyTorch is
+only used to hold device memory and to name the current CUDA stream; every step of the
+quantization runs in the library's CUDA kernels.  There is no CPU fallback: if the
+library is missing or no GPU is present, calls raise.
+
+Typical use::
+
+    import torch, fp8_token_group_gb300 as ptgq
+    x = torch.randn(4096, 7168, device="cuda", dtype=torch.bfloat16)
+    q, s = ptgq.quantize(x, group_size=128, scale_fmt=ptgq.SCALE_UE8M0_PACKED,
+                         scale_layout=ptgq.COL_MAJOR_TMA)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+__all__ = [
+    "BF16", "FP16", "E4M3", "INT8", "SCALE_FP32", "SCALE_UE8M0_PACKED", "SCALE_UE8M0_FP32",
+    "ROW_MAJOR", "COL_MAJOR_TMA", "FLAG_NO_PDL", "FLAG_UE8M0_SCALE_FLOOR", "EPS_MIN",
+    "PtgqError", "lib", "lib_path", "header_functions", "quant", "quantize", "scale_elems",
+    "alloc_outputs", "strerror",
+]
+
+BF16, FP16 = 0, 1
+E4M3, INT8 = 0, 1
+SCALE_FP32, SCALE_UE8M0_PACKED, SCALE_UE8M0_FP32 = 0, 1, 2
+ROW_MAJOR, COL_MAJOR_TMA = 0, 1
+FLAG_NO_PDL, FLAG_UE8M0_SCALE_FLOOR = 1, 2
+EPS_MIN = 1e-24
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_HEADER = os.path.join(os.path.dirname(_HERE), "include", "ptgq.h")
+_lock = threading.Lock()
+_lib = None
+
+
+class PtgqError(RuntimeError):
+    def __init__(self, status: int, what: str = "ptgq_quant"):
+        self.status = status
+        super().__init__(f"{what} failed with status {status}: {strerror(status)}")
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libptgq.so")
+
+
+def header_functions() -> list[str]:
+    """Names of the functions ``include/ptgq.h`` declares."""
+    text = open(_HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(ptgq_\w+)\s*\(", text, re.M)))
+
+
+def lib() -> ctypes.CDLL:
+    """Load libptgq.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+            import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+            L = ctypes.CDLL(path, mode=ctypes.RTLD_GLOBAL)
+            i32, i64, vp, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+            L.ptgq_quant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i32, vp, i32, i32, i32, vp,
+                                     f32, vp]
+            L.ptgq_quant.restype = i32
+            L.ptgq_quant_ex.argtypes = L.ptgq_quant.argtypes + [ctypes.c_uint]
+            L.ptgq_quant_ex.restype = i32
+            L.ptgq_scale_elems.argtypes = [i64, i64, i64, i32, i32, i32, i32,
+                                           ctypes.POINTER(i64)]
+            L.ptgq_scale_elems.restype = i32
+            L.ptgq_strerror.argtypes = [i32]
+            L.ptgq_strerror.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().ptgq_strerror(status).decode()
+
+
+def scale_elems(n: int, tokens_pad: int, hidden: int, group_size: int, scale_fmt: int,
+                scale_layout: int, masked: bool) -> int:
+    out = ctypes.c_int64(0)
+    rc = lib().ptgq_scale_elems(n, tokens_pad, hidden, group_size, scale_fmt, scale_layout,
+                                int(bool(masked)), ctypes.byref(out))
+    if rc != 0:
+        raise PtgqError(rc, "ptgq_scale_elems")
+    return out.value
+
+
+def _in_dtype(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float16:
+        return FP16
+    raise TypeError(f"input must be bfloat16 or float16, got {t.dtype}")
+
+
+def alloc_outputs(x, group_size: int, *, out_dtype: int = E4M3, scale_fmt: int = SCALE_FP32,
+                  scale_layout: int = ROW_MAJOR, fuse_silu: bool = False, masked: bool = False,
+                  tokens_pad: int = 0):
+    """Allocate (out_q, out_s) on x's device for the given configuration."""
+    import torch
+    if masked:
+        E, tp, hin = x.shape
+        n, rows = E, tp
+        tokens_pad = tp
+    else:
+        n, hin = x.shape
+        rows = tokens_pad or n
+    H = hin // 2 if fuse_silu else hin
+    qshape = (n, rows, H) if masked else (rows, H)
+    qdt = torch.float8_e4m3fn if out_dtype == E4M3 else torch.int8
+    q = torch.empty(qshape, dtype=qdt, device=x.device)
+    ns = scale_elems(n, tokens_pad, H, group_size, scale_fmt, scale_layout, masked)
+    sdt = torch.int32 if scale_fmt == SCALE_UE8M0_PACKED else torch.float32
+    s = torch.empty(ns, dtype=sdt, device=x.device)
+    return q, s
+
+
+def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
+          scale_fmt: int = SCALE_FP32, scale_layout: int = ROW_MAJOR, fuse_silu: bool = False,
+          masked_m=None, eps: float = 1e-10, tokens_pad: int = 0, flags: int = 0,
+          stream=None) -> None:
+    """Quantize ``x`` into the caller's ``out_q`` / ``out_s`` (device tensors) on ``stream``
+    (default: torch's current stream).  Arguments follow ``ptgq_quant`` in include/ptgq.h."""
+    import torch
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor (use quantize() for host tensors)")
+    if not (x.is_contiguous() and out_q.is_contiguous() and out_s.is_contiguous()):
+        raise ValueError("x, out_q and out_s must be contiguous")
+    if out_dtype is None:
+        out_dtype = INT8 if out_q.dtype == torch.int8 else E4M3
+    if masked_m is not None:
+        if masked_m.dtype != torch.int32 or not masked_m.is_cuda:
+            raise ValueError("masked_m must be a CUDA int32 tensor")
+        E, tp, hin = x.shape
+        n, tokens_pad = E, tp
+    else:
+        n, hin = x.shape
+    H = hin // 2 if fuse_silu else hin
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    rc = lib().ptgq_quant_ex(
+        x.data_ptr(), _in_dtype(x), n, tokens_pad, H, group_size, out_q.data_ptr(), out_dtype,
+        out_s.data_ptr(), scale_fmt, scale_layout, int(bool(fuse_silu)),
+        None if masked_m is None else masked_m.data_ptr(), float(eps), handle, flags)
+    if rc != 0:
+        raise PtgqError(rc)
+
+
+def quantize(x, group_size: int = 128, *, out_dtype: int = E4M3, scale_fmt: int = SCALE_FP32,
+             scale_layout: int = ROW_MAJOR, fuse_silu: bool = False, masked_m=None,
+             eps: float = 1e-10, tokens_pad: int = 0, flags: int = 0):
+    """Allocate outputs and quantize.  A host (CPU) ``x`` is copied to the current CUDA
+    device, quantized there, and the outputs are copied back to the host."""
+    import torch
+    host = not x.is_cuda
+    xd = x.to("cuda", non_blocking=True) if host else x
+    mm = masked_m
+    if mm is not None and not mm.is_cuda:
+        mm = mm.to("cuda", non_blocking=True)
+    q, s = alloc_outputs(xd, group_size, out_dtype=out_dtype, scale_fmt=scale_fmt,
+                         scale_layout=scale_layout, fuse_silu=fuse_silu,
+                         masked=mm is not None, tokens_pad=tokens_pad)
+    quant(xd, q, s, group_size, out_dtype=out_dtype, scale_fmt=scale_fmt,
+          scale_layout=scale_layout, fuse_silu=fuse_silu, masked_m=mm, eps=eps,
+          tokens_pad=tokens_pad, flags=flags)
+    if host:
+        q, s = q.cpu(), s.cpu()
+    return q, s

@@ -1,0 +1,62 @@
+// ptgq_internal.h -- launch parameters shared by the kernel translation units and the
+// C ABI layer.  Not part of the public interface (that is include/ptgq.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ptgq {
+
+constexpr int kThreads = 256;                 // 8 warps per CTA
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxExperts = 4096;             // masked scheduler: E <= kMaxExperts
+
+// Work decomposition.  A "unit" is one group (float scale formats) or four
+// consecutive groups of one row (packed UE8M0, so one unit fills one int32 word).
+// One lane handles 16 consecutive elements of a group (32 bytes of bf16/fp16),
+// so a group spans G/16 lanes and a unit 4*G/16 or G/16 lanes; a warp task is 32
+// lanes = 32 / (lanes per unit) consecutive units.  Units are numbered row by row
+// over the live rows (flat: all T rows; masked: expert by expert, live rows only).
+struct Params {
+  const void* x;             // input (bf16/fp16)
+  void* q;                   // codes (e4m3/int8)
+  void* s;                   // scales
+  const int32_t* masked_m;   // nullptr: flat scheduler
+  int64_t n;                 // flat: live rows T; masked: experts E
+  int64_t rows;              // rows per block of x/q (flat: tokens_pad or T; masked: tokens_pad)
+  int64_t hidden;            // H
+  int64_t in_row;            // elements per input row (H, or 2H with silu)
+  uint32_t lg_log2;          // log2(lanes per group) = log2(G / 16)
+  uint32_t ug_log2;          // log2(groups per unit): 2 for packed UE8M0, else 0
+  uint32_t ng;               // groups per row
+  uint32_t upr;              // units per row = ceil(ng / groups per unit)
+  uint32_t upr_magic;        // floor(2^32 / upr), or 0xFFFFFFFF when upr == 1
+  uint32_t units_flat;       // flat: T * upr (< 2^32); masked: unused
+  int32_t scale_fmt;         // 0 fp32, 1 packed UE8M0, 2 UE8M0 as fp32
+  int32_t col_major;         // scales column-major (TMA-aligned)
+  int64_t s_ncol;            // scale columns (ng, or ceil(ng/4) words)
+  int64_t s_mn_pad;          // column pitch of the column-major layout
+  int64_t s_per_block;       // scale elements per block (per expert)
+  float eps;                 // amax floor
+  float fmax;                // 448 (e4m3) or 127 (int8)
+  int32_t scale_floor;       // vLLM UE8M0 semantics: s = max(s, 1e-10) before rounding
+  // Flat zero-fill of padding (rows [T, rows) of q; scale rows past T).
+  int64_t zero_q_begin;      // byte offsets into q, multiples of 16
+  int64_t zero_q_end;
+  int64_t zero_s_rows;       // scale rows to zero per column: [T, T + zero_s_rows)
+};
+
+// One kernel instance per (input type, output type, scale arithmetic, silu).
+struct KernelKey {
+  int fp16;       // input is fp16 (else bf16)
+  int int8;       // output is int8 (else e4m3)
+  int pow2;       // UE8M0 scale (multiply by an exact power of two) vs fp32 division
+  int silu;       // fused silu(gate) * up
+};
+
+// Returns the __global__ function of an instance (defined in the instance TUs).
+const void* kernel_for(const KernelKey& k);
+// Dynamic shared memory the instance needs for `experts` masked blocks (0: flat).
+size_t dynamic_smem_bytes(const KernelKey& k, int64_t experts);
+
+}  // namespace ptgq

@@ -1,0 +1,316 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle, element by
+element, on the same seeded inputs.  Non-silu variants must match bit for bit (codes
+and scales, including padding and masked rows); the fused-silu variants are held to the
+stated tolerance (<= 1 e4m3 step on <= 1e-4 of codes, scale relative error <= 2e-7) and,
+separately, checked for the exactness the kernel's correctly rounded exp gives."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_token_group_gb300 as P
+from fp8_token_group_gb300 import synth
+from parity_util import Case, assert_same, compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [P.SCALE_FP32, P.SCALE_UE8M0_PACKED, P.SCALE_UE8M0_FP32]
+LAYOUTS = [P.ROW_MAJOR, P.COL_MAJOR_TMA]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    P.lib()
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_flat_small_bf16_64x4096_fp32_rowmajor():
+    compare(synth.flat_small(), Case())
+
+
+def test_flat_outliers_4096x7168_ue8m0_packed_colmajor():
+    """The benchmarked workload, at full size, in the launch configuration bench.py times."""
+    compare(synth.flat_outliers(), Case(scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA))
+
+
+def test_silu_flat_8192x2x2048_fp32_colmajor():
+    x = synth.silu_flat()
+    c = Case(silu=True, layout=P.COL_MAJOR_TMA)
+    compare(x, c, exact_silu=False)
+    compare(x, c, exact_silu=True)
+
+
+def test_masked_silu_32x384x2x4096_ue8m0_packed_colmajor():
+    x, mm = synth.masked_silu()
+    c = Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA)
+    compare(x, c, masked_m=mm.numpy(), exact_silu=False)
+    compare(x, c, masked_m=mm.numpy(), exact_silu=True)
+
+
+SMALL_SWEEP = [cs for cs in synth.sweep_cases() if cs[1] <= 4096]
+
+
+@pytest.mark.parametrize("idx,T,H,dt,G,out", SMALL_SWEEP,
+                         ids=[f"{c[1]}x{c[2]}-{str(c[3])[6:]}-G{c[4]}-{c[5]}" for c in SMALL_SWEEP])
+def test_sweep(idx, T, H, dt, G, out):
+    x = synth.sweep_input(idx, T, H, dt)
+    compare(x, Case(group=G, out_dtype=P.E4M3 if out == "e4m3" else P.INT8))
+
+
+# 32768 tokens: every hidden size and dtype, with (G=128, e4m3) and (G=16, int8); the
+# other group/output pairs are covered at every smaller token count.
+LARGE_SWEEP = [cs for cs in synth.sweep_cases() if cs[1] > 4096
+               and (cs[4], cs[5]) in ((128, "e4m3"), (16, "int8"))]
+
+
+@pytest.mark.parametrize("idx,T,H,dt,G,out", LARGE_SWEEP,
+                         ids=[f"{c[1]}x{c[2]}-{str(c[3])[6:]}-G{c[4]}-{c[5]}" for c in LARGE_SWEEP])
+def test_sweep_32768_tokens_sampled_rows(idx, T, H, dt, G, out):
+    """Full-size launch; the oracle checks a sample of rows (rows are independent)."""
+    x = synth.sweep_input(idx, T, H, dt)
+    c = Case(group=G, out_dtype=P.E4M3 if out == "e4m3" else P.INT8)
+    gq, gs = run_gpu(x, c)
+    rng = np.random.default_rng(idx)
+    rows = np.unique(np.concatenate([[0, 1, 2, 3, T - 1], rng.choice(T, 252, replace=False)]))
+    oq, os_ = run_oracle(x[torch.from_numpy(rows)].contiguous(), c)
+    ng = H // G
+    assert_same(gq.reshape(T, H)[rows].ravel(), gs.reshape(T, ng)[rows].ravel(), oq, os_,
+                f"sweep {idx} sampled rows")
+
+
+# ---------------------------------------------------------------- the pages' shape grid
+
+@pytest.mark.parametrize("silu", [False, True])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("T", [1, 7, 64, 333])
+@pytest.mark.parametrize("H", [128, 2048, 4096])
+@pytest.mark.parametrize("fmt", [P.SCALE_FP32, P.SCALE_UE8M0_PACKED])
+def test_naive_scheduler_grid(silu, dt, T, H, fmt):
+    """96 flat cases: vanilla and fused silu x bf16/fp16 x T x H x float/UE8M0 scales."""
+    x = synth.normal((T, 2 * H if silu else H), dt, seed=T * 7 + H)
+    compare(x, Case(silu=silu, scale_fmt=fmt, layout=P.COL_MAJOR_TMA), exact_silu=True)
+
+
+@pytest.mark.parametrize("E,H,tp", list(itertools.product([2, 5], [2048, 4096], [128, 384])))
+def test_masked_scheduler_grid(E, H, tp):
+    """8 masked cases: UE8M0 + silu, [E, tokens_pad, 2H]."""
+    x = synth.normal((E, tp, 2 * H), torch.bfloat16, seed=E * 1000 + tp)
+    mm = synth.masked_counts(E, tp, seed=E + tp)
+    compare(x, Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA),
+            masked_m=mm.numpy())
+
+
+# ---------------------------------------------------------------- every variant, ragged shapes
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("out", [P.E4M3, P.INT8])
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("G", [16, 32, 64, 128])
+@pytest.mark.parametrize("silu", [False, True])
+def test_flat_variants_ragged(dt, out, fmt, layout, G, silu):
+    """37 live rows padded to 45, 7 groups per row (a partial packed word)."""
+    H = 7 * G
+    x = synth.sweep_input(3, 37, 2 * H if silu else H, dt)
+    compare(x, Case(group=G, out_dtype=out, scale_fmt=fmt, layout=layout, silu=silu,
+                    tokens_pad=45))
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("out", [P.E4M3, P.INT8])
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("G", [16, 128])
+@pytest.mark.parametrize("silu", [False, True])
+def test_masked_variants(dt, out, fmt, layout, G, silu):
+    """The pages' masked counts {0, 1, 17, m} plus out-of-range values, clamped."""
+    H = 5 * G
+    x = synth.sweep_input(11, 6 * 23, 2 * H if silu else H, dt).reshape(6, 23, -1)
+    mm = np.array([0, 1, 17, 23, 40, -3], dtype=np.int32)
+    compare(x, Case(group=G, out_dtype=out, scale_fmt=fmt, layout=layout, silu=silu),
+            masked_m=mm)
+
+
+# ---------------------------------------------------------------- exhaustive value checks
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("out", [P.E4M3, P.INT8])
+@pytest.mark.parametrize("fmt", [P.SCALE_FP32, P.SCALE_UE8M0_FP32])
+def test_every_16bit_value_with_anchor(dt, out, fmt):
+    """Every finite 16-bit value in a group whose anchor makes the scale exactly 1."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = torch.from_numpy(bits.view(np.int16).copy()).view(dt).float()
+    anchor = 448.0 if out == P.E4M3 else 127.0
+    vals = vals[torch.isfinite(vals) & (vals.abs() <= anchor)]
+    n = -(-vals.numel() // 127)
+    grid = torch.zeros(n * 127)
+    grid[: vals.numel()] = vals
+    x = torch.cat([torch.full((n, 1), anchor), grid.view(n, 127)], 1).to(dt)
+    compare(x, Case(out_dtype=out, scale_fmt=fmt))
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("out", [P.E4M3, P.INT8])
+def test_division_every_quotient_pattern(dt, out):
+    """For every amax mantissa of one binade and every value of up to 24 binades below it
+    (both signs): the kernel's reciprocal-based division gives the IEEE codes.  Scaling by
+    powers of two does not change the rounding, so this covers all normal pairs."""
+    mant_bits = 7 if dt == torch.bfloat16 else 10
+    step = 2.0 ** -mant_bits
+    amaxes = 1.0 + step * np.arange(2 ** mant_bits)
+    vals = []
+    for e in range(0, 24):
+        vals.append((1.0 + step * np.arange(2 ** mant_bits)) * 2.0 ** -e)
+    vals = np.concatenate(vals)
+    vals = np.concatenate([vals, -vals]).astype(np.float32)
+    per = 127
+    n_chunks = -(-vals.size // per)
+    padded = np.zeros(n_chunks * per, np.float32)
+    padded[: vals.size] = vals
+    chunks = padded.reshape(n_chunks, per)
+    rows = []
+    for a in amaxes:
+        ok = np.minimum(np.abs(chunks), a)
+        rows.append(np.concatenate([np.full((n_chunks, 1), a, np.float32),
+                                    np.copysign(ok, chunks)], 1))
+    x = torch.from_numpy(np.concatenate(rows)).to(dt)
+    x = x.reshape(-1, 128 * 4) if x.shape[0] % 4 == 0 else x
+    compare(x, Case(out_dtype=out))
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_silu_every_16bit_gate(dt):
+    """Each gate value is the only non-zero product of its group (up = 1): the fp32 scale
+    is RN(|silu(g)| / 448), so every silu value the kernel produces is compared."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    g = torch.from_numpy(bits.view(np.int16).copy()).view(dt)
+    g = g[torch.isfinite(g.float()) & (g.float().abs() < 1e37)]   # 3 * silu(g) stays finite
+    n = g.numel()
+    gate = torch.zeros((n, 128), dtype=dt)
+    up = torch.zeros((n, 128), dtype=dt)
+    gate[:, 0] = g
+    up[:, 0] = 1.0
+    gate[:, 1] = g            # a second copy scaled by up = -3 checks the product
+    up[:, 1] = -3.0
+    x = torch.cat([gate, up], 1)
+    compare(x, Case(silu=True, eps=1e-24), exact_silu=True)
+
+
+# ---------------------------------------------------------------- edge cases
+
+def test_all_zero_bytes_0x55_and_vllm_floor_0x5e():
+    x = torch.zeros((5, 7168), dtype=torch.bfloat16)
+    c = Case(scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA)
+    gq, gs = compare(x, c)
+    assert np.all(gq == 0) and np.all(gs.reshape(14, 8)[:, :5] == 0x55555555)
+    assert np.all(gs.reshape(14, 8)[:, 5:] == 0)
+    c.flags = P.FLAG_UE8M0_SCALE_FLOOR
+    gq, gs = compare(x, c)
+    assert np.all(gs.reshape(14, 8)[:, :5] == 0x5E5E5E5E)
+
+
+@pytest.mark.parametrize("eps", [1e-24, 1e-10, 1e-4, 1.0, 1e20])
+def test_eps_range(eps):
+    x = synth.sweep_input(5, 64, 1024, torch.bfloat16)
+    x[3] = 0
+    x[5, :128] = 1e-30
+    for fmt in FMTS:
+        compare(x, Case(eps=eps, scale_fmt=fmt))
+
+
+def test_extreme_values():
+    dt = torch.bfloat16
+    x = torch.zeros((8, 256), dtype=dt)
+    x[0, :] = torch.finfo(dt).max
+    x[1, ::2] = -torch.finfo(dt).max
+    x[2, :] = torch.finfo(dt).tiny
+    x[3, :] = 2.0 ** -133              # smallest bf16 subnormal
+    x[4, :] = -0.0
+    x[5, 0] = 3e38
+    x[5, 1:] = 1e-30
+    x[6, :] = torch.linspace(-500, 500, 256).to(dt)
+    x[7, 1::2] = -0.0
+    for out in (P.E4M3, P.INT8):
+        for fmt in FMTS:
+            compare(x, Case(out_dtype=out, scale_fmt=fmt))
+    # silu: extreme gates with up = 1 (gate * up must stay finite)
+    xs = torch.cat([x, torch.ones_like(x)], 1)
+    for fmt in FMTS:
+        compare(xs, Case(silu=True, scale_fmt=fmt), exact_silu=True)
+
+
+def test_flat_zero_tokens_only_zero_fills_padding():
+    x = torch.zeros((0, 1024), dtype=torch.bfloat16)
+    for fmt in FMTS:
+        for layout in LAYOUTS:
+            compare(x, Case(scale_fmt=fmt, layout=layout, tokens_pad=9))
+
+
+def test_masked_all_empty_and_zero_experts():
+    x = synth.normal((3, 16, 256), torch.bfloat16, seed=1)
+    compare(x, Case(), masked_m=np.zeros(3, np.int32))
+    gq, gs = run_gpu(synth.normal((0, 16, 256), torch.bfloat16), Case(),
+                     masked_m=np.zeros(0, np.int32))
+    assert gq.size == 0 and gs.size == 0
+
+
+def test_many_experts():
+    E = 1000
+    x = synth.normal((E, 4, 256), torch.bfloat16, seed=2)
+    mm = synth.masked_counts(E, 4, seed=5).numpy()
+    compare(x, Case(scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA), masked_m=mm)
+
+
+# ---------------------------------------------------------------- launch behaviour
+
+def test_pdl_and_plain_launch_agree_and_repeat():
+    x = synth.flat_outliers(512, 7168)
+    c = Case(scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA)
+    a = run_gpu(x, c)
+    c.flags = P.FLAG_NO_PDL
+    b = run_gpu(x, c)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_back_to_back_launches_and_cuda_graph():
+    x = synth.silu_flat(1024, 2048).cuda()
+    q, s = P.alloc_outputs(x, 128, fuse_silu=True)
+    P.quant(x, q, s, 128, fuse_silu=True)
+    torch.cuda.synchronize()
+    ref_q, ref_s = q.clone(), s.clone()
+    q2, s2 = torch.empty_like(q), torch.empty_like(s)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            P.quant(x, q2, s2, 128, fuse_silu=True)
+    torch.cuda.synchronize()
+    assert torch.equal(q2.view(torch.uint8), ref_q.view(torch.uint8)) and torch.equal(s2, ref_s)
+    q3, s3 = torch.zeros_like(q), torch.zeros_like(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(3):
+            P.quant(x, q3, s3, 128, fuse_silu=True)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(q3.view(torch.uint8), ref_q.view(torch.uint8)) and torch.equal(s3, ref_s)
+
+
+def test_device_arguments_rejected_before_launch():
+    x = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
+    q, s = P.alloc_outputs(x, 128)
+    L = P.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = L.ptgq_quant(x.data_ptr() + 2, 0, 4, 0, 256, 128, q.data_ptr(), 0, s.data_ptr(), 0, 0,
+                      0, None, 1e-10, stream)
+    assert rc == -7
+    rc = L.ptgq_quant(x.data_ptr(), 0, 4, 0, 256, 128, q.data_ptr() + 8, 0, s.data_ptr(), 0, 0,
+                      0, None, 1e-10, stream)
+    assert rc == -7
+    rc = L.ptgq_quant(x.data_ptr(), 0, 4, 2, 256, 128, q.data_ptr(), 0, s.data_ptr(), 0, 0, 0,
+                      None, 1e-10, stream)
+    assert rc == -6
