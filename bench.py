@@ -9,7 +9,8 @@ Prints one JSON line.  ``value`` is the achieved HBM throughput in GB/s (algorit
 input read + codes written + scale words written, per call, over the device time of the
 timed steps, summed over ranks).  Timing: W warm-up steps, then K steps replayed from a
 CUDA graph, bracketed by barrier + synchronize, timed with CUDA events on the launching
-stream; inputs rotate over four buffer sets (353 MB) so each call reads from HBM, not L2.
+stream; inputs rotate over buffer sets that together exceed 2.5x L2, so each call reads
+from HBM, not L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -35,8 +36,7 @@ METRIC = "achieved HBM GB/s (% of GB300 peak) and µs/call, per_token_group_quan
 WORKLOAD = "flat bf16 x[4096,7168] N(0,1)+0.1% outliers x100+1% zero groups, G=128, e4m3, " \
            "UE8M0 packed int32 col-major (mn padded to 4, pads zero-filled)"
 T, H, G = 4096, 7168, 128
-BUFFER_SETS = 4
-GRAPH_CALLS = 400                      # calls captured per CUDA graph (a multiple of BUFFER_SETS)
+GRAPH_CALLS = 400                      # calls captured per CUDA graph
 KERNEL_SOURCES = ["ptgq_kernel.cuh", "ptgq_math.cuh", "ptgq_api.cu", "ptgq_internal.h",
                   "ptgq_inst_bf16.cu", "silu_tables.inc"]
 
@@ -220,39 +220,100 @@ def run_reference(args, world, rank):
     return 0
 
 
+# ---------------------------------------------------------------- workloads
+
+L2_BYTES = 129 * 2 ** 20
+
+
+class Workload:
+    """One configuration: seeded CPU input, quantization arguments, algorithmic bytes."""
+
+    def __init__(self, name, desc, make, *, silu=False, fmt=0, layout=0, group=G, out=0):
+        self.name, self.desc, self.make = name, desc, make
+        self.silu, self.fmt, self.layout, self.group, self.out = silu, fmt, layout, group, out
+
+    def inputs(self):
+        r = self.make()
+        return r if isinstance(r, tuple) else (r, None)
+
+    def live_rows(self, x, mm) -> int:
+        if mm is None:
+            return x.shape[0]
+        return int(mm.clamp(0, x.shape[1]).sum())
+
+    def bytes_per_call(self, x, mm) -> int:
+        hin = x.shape[-1]
+        h = hin // 2 if self.silu else hin
+        live = self.live_rows(x, mm)
+        ng = h // self.group
+        if self.fmt == 1:   # packed UE8M0: int32 words, column pitch round_up(rows, 4)
+            ncol = (ng + 3) // 4
+            rows = x.shape[1] if mm is not None else (x.shape[0] + 3) // 4 * 4
+            sbytes = 4 * ncol * (live if mm is not None else rows)
+        else:
+            sbytes = 4 * ng * live
+        return live * hin * 2 + live * h + sbytes
+
+    def call(self, P, xd, q, s, mm=None):
+        P.quant(xd, q, s, self.group, out_dtype=self.out, scale_fmt=self.fmt,
+                scale_layout=self.layout, fuse_silu=self.silu, masked_m=mm)
+
+    def alloc(self, P, xd, mm):
+        return P.alloc_outputs(xd, self.group, out_dtype=self.out, scale_fmt=self.fmt,
+                               scale_layout=self.layout, fuse_silu=self.silu,
+                               masked=mm is not None)
+
+
+def workloads():
+    from fp8_token_group_gb300 import synth
+    import torch
+    return {
+        "flat_outliers": Workload("flat_outliers", WORKLOAD, synth.flat_outliers, fmt=1, layout=1),
+        "flat_small": Workload("flat_small", "flat bf16 x[64,4096] N(0,1), G=128, e4m3, fp32 "
+                               "row-major scales [64,32]", synth.flat_small),
+        "silu_flat": Workload("silu_flat", "fused silu*up, bf16 [8192, 2x2048] -> e4m3 "
+                              "[8192,2048], G=128, fp32 column-major scales [32,8192]",
+                              synth.silu_flat, silu=True, layout=1),
+        "masked_silu": Workload("masked_silu", "masked EP-MoE bf16 [32,384,2x4096], masked_m "
+                                "uniform in [0,384], fused silu, G=128, e4m3, UE8M0 packed "
+                                "column-major", synth.masked_silu, silu=True, fmt=1, layout=1),
+        "sweep_big": Workload("sweep_big", "flat bf16 [32768,7168] N(0,1), G=128, e4m3, fp32 "
+                              "row-major", lambda: synth.normal((32768, 7168), torch.bfloat16,
+                                                                seed=1)),
+    }
+
+
 # ---------------------------------------------------------------- GPU timing
 
-def build_sets(x_cpu, device):
-    import torch
-    import fp8_token_group_gb300 as P
+def build_sets(P, wl, x_cpu, mm_cpu, device):
+    """Enough buffer sets (each with its own input copy) that together they exceed L2 2.5x."""
+    per_set = wl.bytes_per_call(x_cpu, mm_cpu)
+    nsets = max(2, min(GRAPH_CALLS, -(-int(2.5 * L2_BYTES) // max(per_set, 1))))
+    while GRAPH_CALLS % nsets:
+        nsets += 1
+    mm = None if mm_cpu is None else mm_cpu.to(device)
     sets = []
-    for _ in range(BUFFER_SETS):
+    for _ in range(nsets):
         xd = x_cpu.to(device)
-        q, s = P.alloc_outputs(xd, G, scale_fmt=P.SCALE_UE8M0_PACKED,
-                               scale_layout=P.COL_MAJOR_TMA)
-        sets.append((xd, q, s))
+        q, s = wl.alloc(P, xd, mm)
+        sets.append((xd, q, s, mm))
     return sets
 
 
-def call(P, st):
-    xd, q, s = st
-    P.quant(xd, q, s, G, scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
-
-
-def time_graph(P, sets, steps: int, warmup: int, world: int, sampler=None):
+def time_graph(P, wl, sets, steps: int, warmup: int, world: int, sampler=None):
     """Capture GRAPH_CALLS calls (rotating buffer sets) and replay; returns elapsed s for
-    `steps` calls (rounded up to whole graphs) and the number of calls made."""
+    `steps` calls (rounded up to whole graphs), the number of calls made, and clocks."""
     import torch
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
-        for i in range(8):
-            call(P, sets[i % len(sets)])
+        for i in range(min(8, len(sets))):
+            wl.call(P, *sets[i])
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(GRAPH_CALLS):
-            call(P, sets[i % len(sets)])
+            wl.call(P, *sets[i % len(sets)])
     reps = max(1, -(-steps // GRAPH_CALLS))
     wreps = max(1, -(-warmup // GRAPH_CALLS))
     with torch.cuda.stream(stream):
@@ -272,21 +333,23 @@ def time_graph(P, sets, steps: int, warmup: int, world: int, sampler=None):
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
+    del g
     return start.elapsed_time(end) / 1e3, reps * GRAPH_CALLS, clocks
 
 
-def time_e2e(P, x_cpu, steps: int, device):
+def time_e2e(P, wl, x_cpu, mm_cpu, steps: int, device):
     """Public API with host buffers: per step H2D of x (pinned), quantize, D2H of q and s."""
     import torch
     xh = x_cpu.pin_memory()
     xd = torch.empty_like(xh, device=device)
-    q, s = P.alloc_outputs(xd, G, scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
+    mm = None if mm_cpu is None else mm_cpu.to(device)
+    q, s = wl.alloc(P, xd, mm)
     qh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     sh = torch.empty(s.shape, dtype=s.dtype).pin_memory()
 
     def step():
         xd.copy_(xh, non_blocking=True)
-        P.quant(xd, q, s, G, scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
+        wl.call(P, xd, q, s, mm)
         qh.copy_(q, non_blocking=True)
         sh.copy_(s, non_blocking=True)
 
@@ -305,103 +368,53 @@ def time_e2e(P, x_cpu, steps: int, device):
     return el, h2d, d2h
 
 
-def other_workloads(P, device, steps: int) -> dict:
-    """Device throughput of the other large workloads (context for the roofline; each is a
-    parity-tested configuration, not a bench line)."""
+def measure_device(P, wl, device, steps: int) -> dict:
     import torch
-    from fp8_token_group_gb300 import synth
-    out = {}
-
-    def measure(name, make, nbytes, nsets):
-        sets = [make() for _ in range(nsets)]
-        stream = torch.cuda.Stream()
-        stream.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(stream):
-            for i in range(6):
-                sets[i % nsets][0]()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(100):
-                sets[i % nsets][0]()
-        with torch.cuda.stream(stream):
-            g.replay()
-        torch.cuda.synchronize()
-        reps = max(1, steps // 100)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a.record(stream)
-            for _ in range(reps):
-                g.replay()
-            b.record(stream)
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (reps * 100)
-        nb = nbytes(sets[0][1])
-        out[name] = {"us_per_call": round(us, 3), "bytes_per_call": nb,
-                     "gbs": round(nb / us / 1e3, 1)}
-
-    # Each buffer set has its own input copy, so the sets together exceed L2.
-    # fused silu, flat bf16 [8192, 2x2048] -> e4m3 [8192, 2048], fp32 column-major scales
-    xs_cpu = synth.silu_flat()
-
-    def mk_silu():
-        xs = xs_cpu.to(device)
-        q, s = P.alloc_outputs(xs, G, fuse_silu=True, scale_layout=P.COL_MAJOR_TMA)
-        return (lambda: P.quant(xs, q, s, G, fuse_silu=True, scale_layout=P.COL_MAJOR_TMA)), None
-    measure("silu_flat_8192x2x2048", mk_silu,
-            lambda _: 8192 * 4096 * 2 + 8192 * 2048 + 32 * 8192 * 4, 4)
-
-    # masked silu, bf16 [32, 384, 2x4096], UE8M0 packed column-major
-    xm_cpu, mm = synth.masked_silu()
-    mmd = mm.to(device)
-    live = int(mm.clamp(0, 384).sum())
-
-    def mk_masked():
-        xm = xm_cpu.to(device)
-        q, s = P.alloc_outputs(xm, G, fuse_silu=True, masked=True,
-                               scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
-        return (lambda: P.quant(xm, q, s, G, fuse_silu=True, masked_m=mmd,
-                                scale_fmt=P.SCALE_UE8M0_PACKED,
-                                scale_layout=P.COL_MAJOR_TMA)), None
-    measure(f"masked_silu_32x384x2x4096_live{live}", mk_masked,
-            lambda _: live * (4096 * 2 * 2 + 4096 + 8 * 4), 2)
-
-    # sweep corner: bf16 [32768, 7168], G=128, e4m3, fp32 row-major (input > L2)
-    xb_cpu = synth.normal((32768, 7168), torch.bfloat16, seed=1)
-
-    def mk_big():
-        xb = xb_cpu.to(device)
-        q, s = P.alloc_outputs(xb, G)
-        return (lambda: P.quant(xb, q, s, G)), None
-    measure("sweep_32768x7168_G128_e4m3", mk_big, lambda _: 32768 * 7168 * 3 + 32768 * 56 * 4, 1)
+    x, mm = wl.inputs()
+    sets = build_sets(P, wl, x, mm, device)
+    el, calls, _ = time_graph(P, wl, sets, steps, 100, 1)
+    nb = wl.bytes_per_call(x, mm)
+    us = el / calls * 1e6
+    del sets
     torch.cuda.empty_cache()
-    return out
+    return {"desc": wl.desc, "us_per_call": round(us, 3), "bytes_per_call": nb,
+            "gbs": round(nb / us / 1e3, 1), "live_rows": wl.live_rows(x, mm)}
 
 
 def run_ours(args, world, rank, local):
     import torch
     import fp8_token_group_gb300 as P
-    from fp8_token_group_gb300 import synth
 
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     P.lib()
-    x = synth.flat_outliers()
-    sets = build_sets(x, device)
+    wls = workloads()
+    wl = wls[args.workload]
+    x, mm = wl.inputs()
+    sets = build_sets(P, wl, x, mm, device)
+    nsets = len(sets)
     sampler = ClockSampler(local) if rank == 0 else None
-    elapsed, calls, clocks = time_graph(P, sets, args.steps, args.warmup, world, sampler)
+    elapsed, calls, clocks = time_graph(P, wl, sets, args.steps, args.warmup, world, sampler)
+    del sets
+    torch.cuda.empty_cache()
     max_el = reduce_max(elapsed, world, device)
-    bpc = algorithmic_bytes()
+    bpc = wl.bytes_per_call(x, mm)
     value = aggregate(bpc, calls, world, max_el)
     us = max_el / calls * 1e6
     peak, peak_kind = measured_peak()
     achieved = bpc / (elapsed / calls) / 1e9      # this rank's launches, per launch
 
-    e2e_el, h2d, d2h = time_e2e(P, x, max(3, min(args.steps, 50)), device)
-    e2e_el = reduce_max(e2e_el, world, device)
     e2e_steps = max(3, min(args.steps, 50))
-    others = other_workloads(P, device, 2000) if (rank == 0 and not args.no_extra) else {}
-    base = cpu_baseline(x) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    e2e_el, h2d, d2h = time_e2e(P, wl, x, mm, e2e_steps, device)
+    e2e_el = reduce_max(e2e_el, world, device)
+    others = {}
+    if rank == 0 and not args.no_extra:
+        for name, other in wls.items():
+            if name != wl.name:
+                others[name] = measure_device(P, other, device, 4000)
+    base = cpu_baseline(x) if (rank == 0 and world == 1 and not args.no_cpu
+                               and wl.name == "flat_outliers") else None
+    live = wl.live_rows(x, mm)
 
     if rank == 0:
         line = {
@@ -409,20 +422,20 @@ def run_ours(args, world, rank, local):
             "steps": calls, "warmup": args.warmup, "ms_per_step": round(max_el / calls * 1e3, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": T * world, "hidden": H,
-                       "group_size": G, "input": "bf16", "output": "e4m3",
+            "config": {"workload": wl.desc, "global_batch": live * world, "group_size": wl.group,
+                       "input": "bf16", "output": "e4m3",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": f"{BUFFER_SETS} rotating buffer sets "
-                             f"({BUFFER_SETS * bpc / 1e6:.0f} MB > 129 MB L2)",
+                       "l2": f"{nsets} rotating buffer sets, each with its own input, "
+                             f"together {nsets * bpc / 1e6:.0f} MB > 2.5x the 129 MB L2",
                        "timing": f"CUDA graph of {GRAPH_CALLS} calls replayed, CUDA events"},
             "us_per_call": round(us, 3),
-            "tokens_per_s": round(world * T * calls / max_el, 1),
+            "tokens_per_s": round(world * live * calls / max_el, 1),
             "pct_of_peak": round(100 * achieved / peak, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "traffic": recorded_traffic(),
+                         "traffic": recorded_traffic() if wl.name == "flat_outliers" else None,
                          "algorithmic_bytes_per_launch": bpc},
             "clocks": clocks,
             "gpu_launches": calls,
@@ -446,6 +459,10 @@ def main():
     ap.add_argument("--steps", type=int, default=60000)
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="flat_outliers",
+                    choices=["flat_outliers", "flat_small", "silu_flat", "masked_silu",
+                             "sweep_big"], help="workload of the JSON line (default: the "
+                    "benchmarked flat_outliers)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()

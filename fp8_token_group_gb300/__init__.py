@@ -144,6 +144,8 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
             raise ValueError("masked_m must be a CUDA int32 tensor")
         E, tp, hin = x.shape
         n, tokens_pad = E, tp
+        if E == 0:
+            return      # no experts: nothing to read or write (an empty masked_m has no address)
     else:
         n, hin = x.shape
     H = hin // 2 if fuse_silu else hin

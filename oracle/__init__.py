@@ -63,6 +63,13 @@ def lib() -> ctypes.CDLL:
             L.oracle_quant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i32, vp, i32, i32, i32, vp,
                                        f32, i32]
             L.oracle_quant.restype = i32
+            L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_decode.restype = f32
+            L.oracle_per_token_quant.argtypes = [vp, i32, i64, i64, vp, vp]
+            L.oracle_per_token_quant.restype = i32
+            L.oracle_requant_per_tensor.argtypes = [vp, vp, i64, i64, i64, vp, f32, vp, i64, i64,
+                                                    i64, i32]
+            L.oracle_requant_per_tensor.restype = i32
             _lib = L
     return _lib
 
@@ -128,3 +135,34 @@ def e4m3_encode(y: float) -> int:
 
 def int8_encode(y: float) -> int:
     return lib().oracle_int8_encode(y)
+
+
+def e4m3_decode(c: int) -> float:
+    return lib().oracle_e4m3_decode(c)
+
+
+IN_FP32 = 2
+
+
+def per_token_quant(x: np.ndarray, in_dtype: int, out_q: np.ndarray, out_s: np.ndarray) -> None:
+    """Per-token FP8 quantization of the rows of x ([T, hidden]: uint16 bit patterns for
+    bf16/fp16, float32 for IN_FP32) into out_q (uint8, >= T rows) / out_s (float32)."""
+    assert x.flags.c_contiguous and out_q.dtype == np.uint8 and out_s.dtype == np.float32
+    T, hidden = x.shape
+    rc = lib().oracle_per_token_quant(_ptr(x), in_dtype, T, hidden, _ptr(out_q), _ptr(out_s))
+    if rc != 0:
+        raise ValueError("oracle_per_token_quant rejected its arguments")
+
+
+def requant_per_tensor(x: np.ndarray, x_scale: np.ndarray, strides, masked_m: np.ndarray,
+                       output_scale: float, out: np.ndarray, group_size: int = 128) -> None:
+    """Requantize e4m3 codes x [E, M, K] with per-token-group scales (element strides
+    `strides` = (e, m, g) into x_scale) to one per-tensor scale, rows < masked_m only."""
+    assert x.dtype == np.uint8 and out.dtype == np.uint8 and x_scale.dtype == np.float32
+    E, M, K = x.shape
+    mm = np.ascontiguousarray(masked_m, dtype=np.int32)
+    rc = lib().oracle_requant_per_tensor(_ptr(x), _ptr(x_scale), strides[0], strides[1],
+                                         strides[2], _ptr(mm), float(output_scale), _ptr(out),
+                                         E, M, K, group_size)
+    if rc != 0:
+        raise ValueError("oracle_requant_per_tensor rejected its arguments")

@@ -126,6 +126,15 @@ int8_t int8_encode(float y) {
   return static_cast<int8_t>(r);
 }
 
+// Value of an e4m3fn code, from the format definition (NaN for 0x7F / 0xFF).
+float e4m3_decode(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = e == 0 ? std::ldexp(static_cast<double>(m), -9)
+                          : std::ldexp(1.0 + m / 8.0, e - 7);
+  return static_cast<float>(sign ? -v : v);
+}
+
 // ---- layouts -----------------------------------------------------------------
 
 enum { IN_BF16 = 0, IN_FP16 = 1 };
@@ -175,6 +184,7 @@ bool valid_args(int in_dtype, int64_t n, int64_t tokens_pad, int64_t hidden, int
 extern "C" {
 
 float oracle_bf16_to_float(uint16_t h) { return bf16_to_float(h); }
+float oracle_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
 float oracle_fp16_to_float(uint16_t h) { return fp16_to_float(h); }
 float oracle_exp_f32(float x) { return exp_f32(x); }
 float oracle_silu_mul(float g, float u) { return silu_mul(g, u); }
@@ -297,6 +307,63 @@ int oracle_quant(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens_pad,
           else sf[scale_index(sg, scale_layout, r, c)] = 0.0f;
         }
     }
+  }
+  return 0;
+}
+
+// Per-token (whole-row) FP8 quantization ([sglang#34257], "Key source snippets": the
+// warp kernel).  For each of the first num_tokens rows:
+//   s   = max_i |x_i| / 448                  (no eps floor)
+//   inv = s == 0 ? 0 : 1 / s                 (an all-zero row gets scale 0, codes 0)
+//   q_i = e4m3(clamp(x_i * inv, -448, 448))  (multiplication by the reciprocal)
+// out_s[r] = s.  Rows of out_q / out_s past num_tokens are not touched (the padded
+// output contract of the same page).  in_dtype: 0 bf16, 1 fp16, 2 fp32.
+int oracle_per_token_quant(const void* x, int in_dtype, int64_t num_tokens, int64_t hidden,
+                           uint8_t* out_q, float* out_s) {
+  if (in_dtype < 0 || in_dtype > 2 || num_tokens < 0 || hidden <= 0) return -1;
+  for (int64_t r = 0; r < num_tokens; ++r) {
+    auto val = [&](int64_t i) -> float {
+      const int64_t k = r * hidden + i;
+      if (in_dtype == 2) return static_cast<const float*>(x)[k];
+      return load_elem(static_cast<const uint16_t*>(x) + k, in_dtype);
+    };
+    float m = 0.0f;
+    for (int64_t i = 0; i < hidden; ++i) m = std::fmax(m, std::fabs(val(i)));
+    const float s = m / 448.0f;
+    const float inv = s == 0.0f ? 0.0f : 1.0f / s;
+    for (int64_t i = 0; i < hidden; ++i) {
+      float y = val(i) * inv;
+      y = std::fmin(std::fmax(y, -448.0f), 448.0f);
+      out_q[r * hidden + i] = e4m3_encode(y);
+    }
+    out_s[r] = s;
+  }
+  return 0;
+}
+
+// Per-token-group FP8 -> per-tensor FP8 requantization over the masked EP-MoE layout
+// ([sglang#35593], "Key source snippets": the requant kernel).  x holds e4m3 codes
+// [E, M, K]; x_scale[e, m, k / group] (strides in elements) is the per-token-group scale;
+// for rows m < clamp(masked_m[e], 0, M):
+//   out = e4m3_satfinite((decode(x) * x_scale) * (1 / output_scale))
+// Rows past masked_m are not touched.
+int oracle_requant_per_tensor(const uint8_t* x, const float* x_scale, int64_t stride_e,
+                              int64_t stride_m, int64_t stride_g, const int32_t* masked_m,
+                              float output_scale, uint8_t* out, int64_t E, int64_t M, int64_t K,
+                              int group_size) {
+  if (E < 0 || M < 0 || K <= 0 || group_size <= 0 || K % group_size != 0) return -1;
+  const float inv = 1.0f / output_scale;
+  for (int64_t e = 0; e < E; ++e) {
+    int64_t live = masked_m[e];
+    if (live < 0) live = 0;
+    if (live > M) live = M;
+    for (int64_t m = 0; m < live; ++m)
+      for (int64_t k = 0; k < K; ++k) {
+        const int64_t i = (e * M + m) * K + k;
+        const float sc = x_scale[e * stride_e + m * stride_m + (k / group_size) * stride_g];
+        const float y = (e4m3_decode(x[i]) * sc) * inv;
+        out[i] = e4m3_encode(y);
+      }
   }
   return 0;
 }
