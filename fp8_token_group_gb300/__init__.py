@@ -20,13 +20,13 @@ import re
 import threading
 
 __all__ = [
-    "BF16", "FP16", "E4M3", "INT8", "SCALE_FP32", "SCALE_UE8M0_PACKED", "SCALE_UE8M0_FP32",
+    "BF16", "FP16", "FP32", "E4M3", "INT8", "SCALE_FP32", "SCALE_UE8M0_PACKED", "SCALE_UE8M0_FP32",
     "ROW_MAJOR", "COL_MAJOR_TMA", "FLAG_NO_PDL", "FLAG_UE8M0_SCALE_FLOOR", "EPS_MIN",
     "PtgqError", "lib", "lib_path", "header_functions", "quant", "quantize", "scale_elems",
-    "alloc_outputs", "strerror",
+    "alloc_outputs", "strerror", "per_token_quant", "requant_per_tensor",
 ]
 
-BF16, FP16 = 0, 1
+BF16, FP16, FP32 = 0, 1, 2
 E4M3, INT8 = 0, 1
 SCALE_FP32, SCALE_UE8M0_PACKED, SCALE_UE8M0_FP32 = 0, 1, 2
 ROW_MAJOR, COL_MAJOR_TMA = 0, 1
@@ -75,6 +75,11 @@ def lib() -> ctypes.CDLL:
             L.ptgq_scale_elems.argtypes = [i64, i64, i64, i32, i32, i32, i32,
                                            ctypes.POINTER(i64)]
             L.ptgq_scale_elems.restype = i32
+            L.ptgq_per_token_quant.argtypes = [vp, i32, i64, i64, vp, vp, vp]
+            L.ptgq_per_token_quant.restype = i32
+            L.ptgq_requant_per_tensor.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp, i64, i64,
+                                                  i64, i32, vp]
+            L.ptgq_requant_per_tensor.restype = i32
             L.ptgq_strerror.argtypes = [i32]
             L.ptgq_strerror.restype = ctypes.c_char_p
             _lib = L
@@ -180,3 +185,46 @@ def quantize(x, group_size: int = 128, *, out_dtype: int = E4M3, scale_fmt: int 
     if host:
         q, s = q.cpu(), s.cpu()
     return q, s
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def per_token_quant(x, out_q, out_s, *, num_tokens: int | None = None, stream=None) -> None:
+    """Per-token FP8 quantization of the first ``num_tokens`` rows of x [T, hidden]
+    (bf16/fp16/fp32) into out_q (e4m3, may have more rows) and out_s (float32, one per row).
+    Rows past num_tokens are not touched.  Follows ``ptgq_per_token_quant``."""
+    import torch
+    if not (x.is_cuda and x.is_contiguous() and out_q.is_contiguous() and out_s.is_contiguous()):
+        raise ValueError("x, out_q, out_s must be contiguous CUDA tensors")
+    dt = {torch.bfloat16: BF16, torch.float16: FP16, torch.float32: FP32}.get(x.dtype)
+    if dt is None:
+        raise TypeError(f"unsupported dtype {x.dtype}")
+    T, hidden = x.shape
+    n = T if num_tokens is None else num_tokens
+    rc = lib().ptgq_per_token_quant(x.data_ptr(), dt, n, hidden, out_q.data_ptr(),
+                                    out_s.data_ptr(), _stream_handle(stream, x.device))
+    if rc != 0:
+        raise PtgqError(rc, "ptgq_per_token_quant")
+
+
+def requant_per_tensor(x, x_scale, masked_m, output_scale, out, *, group_size: int = 128,
+                       stream=None) -> None:
+    """Per-token-group FP8 -> per-tensor FP8 requant of x [E, M, K] (e4m3 codes) with
+    x_scale indexed [e, m, k // group_size] through its strides; rows below masked_m[e]
+    only (all rows when masked_m is None); output_scale is a 1-element float32 device
+    tensor.  Follows ``ptgq_requant_per_tensor``."""
+    if not (x.is_cuda and x.is_contiguous() and out.is_contiguous()):
+        raise ValueError("x and out must be contiguous CUDA tensors")
+    E, M, K = x.shape
+    se, sm, sg = x_scale.stride()
+    rc = lib().ptgq_requant_per_tensor(
+        x.data_ptr(), x_scale.data_ptr(), se, sm, sg,
+        None if masked_m is None or E == 0 else masked_m.data_ptr(), output_scale.data_ptr(),
+        out.data_ptr(), E, M, K, group_size, _stream_handle(stream, x.device))
+    if rc != 0:
+        raise PtgqError(rc, "ptgq_requant_per_tensor")

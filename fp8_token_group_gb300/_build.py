@@ -10,8 +10,9 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libptgq.so")
-SOURCES = ["ptgq_api.cu", "ptgq_inst_bf16.cu", "ptgq_inst_fp16.cu"]
-HEADERS = ["ptgq_internal.h", "ptgq_kernel.cuh", "ptgq_math.cuh", "silu_tables.inc"]
+SOURCES = ["ptgq_api.cu", "ptgq_inst_bf16.cu", "ptgq_inst_fp16.cu", "ptgq_next.cu"]
+HEADERS = ["ptgq_internal.h", "ptgq_kernel.cuh", "ptgq_device.cuh", "ptgq_math.cuh",
+           "silu_tables.inc"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast-math: IEEE division/reciprocal, no denormal flushing, and no implicit
 # multiply-add contraction (the kernels write every fused multiply-add explicitly).

@@ -1,0 +1,335 @@
+// ptgq_next.cu -- the two neighbouring operations of the quantizer (sm_103a):
+//
+//  * per-token (whole-row) FP8 quantization (sglang PR #34257, "Key source
+//    snippets": the per-token warp kernel): s = max|x| / 448 per row, inv = 1/s
+//    (0 for an all-zero row), q = e4m3(clamp(x * inv)); rows past num_tokens of a
+//    padded output are not touched.
+//  * per-token-group FP8 -> per-tensor FP8 requantization over the masked EP-MoE
+//    layout (sglang PR #35593, "Key source snippets": the requant kernel):
+//    out = e4m3_satfinite((decode(x) * x_scale[group]) * (1 / output_scale)) for rows
+//    below masked_m[e]; other rows are not touched.
+//
+// Both are streaming kernels bound by HBM bandwidth: persistent grids, full-width
+// vector loads and stores, PDL, no shared-memory staging beyond the masked prefix.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <map>
+#include <tuple>
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include "../../include/ptgq.h"
+#include "ptgq_device.cuh"
+#include "ptgq_internal.h"
+
+namespace ptgq {
+
+// ---------------------------------------------------------------- per-token quant
+
+struct PerTokenParams {
+  const void* x;
+  uint8_t* q;
+  float* s;
+  int64_t tokens;
+  int64_t hidden;
+};
+
+// kIn: 0 bf16, 1 fp16, 2 fp32.  kVecBytes: bytes per lane per load (16, or 8 for 16-bit
+// rows whose length is only a multiple of 4).  Each warp owns one row at a time; the
+// first kCache vectors of each lane stay in registers between the max pass and the
+// quantize pass, the rest are read again (from L2).
+template <int kIn, int kVecBytes>
+__global__ void __launch_bounds__(kThreads) per_token_kernel(const PerTokenParams p) {
+  constexpr int kElems = kIn == 2 ? kVecBytes / 4 : kVecBytes / 2;   // elements per vector
+  constexpr int kWords = kVecBytes / 4;
+  constexpr int kCache = 8;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t nvec = p.hidden / kElems;
+  const char* xb = static_cast<const char*>(p.x);
+
+  auto load = [&](int64_t row, int64_t i, uint32_t (&w)[kWords]) {
+    const char* ptr = xb + (row * p.hidden + i * kElems) * (kIn == 2 ? 4 : 2);
+    if constexpr (kVecBytes == 16) {
+      asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(ptr));
+    } else {
+      asm volatile("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(ptr));
+    }
+  };
+  auto absmax = [&](const uint32_t (&w)[kWords]) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) {
+      if constexpr (kIn == 2) {
+        m = max(m, w[k] & 0x7FFFFFFFu);
+      } else {
+        const uint32_t h = w[k] & 0x7FFF7FFFu;
+        const uint32_t hm = max(h & 0xFFFFu, h >> 16);
+        m = max(m, f2u(kIn == 1 ? widen_lo<true>(hm) : widen_lo<false>(hm)));
+      }
+    }
+    return m;
+  };
+  auto quantize_store = [&](int64_t row, int64_t i, const uint32_t (&w)[kWords], float inv) {
+    float v[kElems];
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) {
+      if constexpr (kIn == 2) {
+        v[k] = u2f(w[k]);
+      } else {
+        v[2 * k] = kIn == 1 ? widen_lo<true>(w[k]) : widen_lo<false>(w[k]);
+        v[2 * k + 1] = kIn == 1 ? widen_hi<true>(w[k]) : widen_hi<false>(w[k]);
+      }
+    }
+    uint32_t o[kElems / 4];
+#pragma unroll
+    for (int k = 0; k < kElems / 4; ++k)
+      o[k] = e4m3x4(__fmul_rn(v[4 * k], inv), __fmul_rn(v[4 * k + 1], inv),
+                    __fmul_rn(v[4 * k + 2], inv), __fmul_rn(v[4 * k + 3], inv));
+    uint8_t* dst = p.q + row * p.hidden + i * kElems;
+    if constexpr (kElems == 8) {
+      asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(o[0]), "r"(o[1]) : "memory");
+    } else {
+      asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(o[0]) : "memory");
+    }
+  };
+
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+       row < p.tokens; row += warps) {
+    uint32_t cache[kCache][kWords];
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < kCache; ++j) {
+      const int64_t i = lane + 32 * j;
+      if (i < nvec) {
+        load(row, i, cache[j]);
+        m = max(m, absmax(cache[j]));
+      }
+    }
+    for (int64_t i = lane + 32 * kCache; i < nvec; i += 32) {
+      uint32_t w[kWords];
+      load(row, i, w);
+      m = max(m, absmax(w));
+    }
+    m = redux_max(m, 0xFFFFFFFFu);
+    const float s = __fdiv_rn(u2f(m), 448.0f);
+    const float inv = s == 0.0f ? 0.0f : __frcp_rn(s);
+#pragma unroll
+    for (int j = 0; j < kCache; ++j) {
+      const int64_t i = lane + 32 * j;
+      if (i < nvec) quantize_store(row, i, cache[j], inv);
+    }
+    for (int64_t i = lane + 32 * kCache; i < nvec; i += 32) {
+      uint32_t w[kWords];
+      load(row, i, w);
+      quantize_store(row, i, w, inv);
+    }
+    if (lane == 0) p.s[row] = s;
+  }
+}
+
+// ---------------------------------------------------------------- requant
+
+struct RequantParams {
+  const uint8_t* x;
+  const float* x_scale;
+  const int32_t* masked_m;       // nullptr: every row is live
+  const float* output_scale;     // device scalar
+  uint8_t* out;
+  int64_t experts;
+  int64_t m;                     // rows per expert
+  int64_t k;                     // row length
+  int64_t se, sm, sg;            // x_scale strides (elements)
+  uint32_t lg_log2;              // log2(lanes per group) = log2(G / 16)
+  uint32_t gpr;                  // groups per row
+  uint32_t gpr_magic;            // floor(2^32 / gpr), or 0xFFFFFFFF when gpr == 1
+};
+
+// Each lane requantizes 16 codes (16 bytes) of one group; G/16 lanes share a group's scale.
+__global__ void __launch_bounds__(kThreads) requant_kernel(const RequantParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem);
+  griddep_wait();
+  griddep_launch_dependents();
+  const bool masked = p.masked_m != nullptr;
+  uint32_t live_rows = static_cast<uint32_t>(p.experts * p.m);
+  if (masked) masked_prefix(p.masked_m, p.experts, p.m, prefix);
+  __syncthreads();
+  if (masked) live_rows = static_cast<uint32_t>(prefix[p.experts]);
+  const float inv = __frcp_rn(*p.output_scale);
+
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t lg = 1u << p.lg_log2;
+  const uint32_t kk = lane & (lg - 1u);
+  const uint32_t gpw_log2 = 5u - p.lg_log2;                 // groups per warp task
+  const uint32_t total_groups = live_rows * p.gpr;
+  const uint32_t tasks = (total_groups + (1u << gpw_log2) - 1u) >> gpw_log2;
+  const uint32_t stride = gridDim.x * kWarps;
+  for (uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < tasks; t += stride) {
+    const uint32_t gi = (t << gpw_log2) + (lane >> p.lg_log2);
+    if (gi >= total_groups) continue;
+    const uint32_t R = udiv(gi, p.gpr, p.gpr_magic);
+    const uint32_t g = gi - R * p.gpr;
+    int64_t e = 0, r = R;
+    if (masked) {
+      e = expert_of(prefix, static_cast<int>(p.experts), R);
+      r = R - prefix[e];
+    } else {
+      e = R / p.m;
+      r = R - e * p.m;
+    }
+    const int64_t off = (e * p.m + r) * p.k + (static_cast<int64_t>(g) << (p.lg_log2 + 4)) + kk * 16;
+    uint32_t w[4];
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p.x + off));
+    const float sc = p.x_scale[e * p.se + r * p.sm + static_cast<int64_t>(g) * p.sg];
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float v[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t f16x2;
+        const uint16_t pair = static_cast<uint16_t>(w[i] >> (16 * h));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+        v[2 * h] = __fmul_rn(__fmul_rn(widen_lo<true>(f16x2), sc), inv);
+        v[2 * h + 1] = __fmul_rn(__fmul_rn(widen_hi<true>(f16x2), sc), inv);
+      }
+      o[i] = e4m3x4(v[0], v[1], v[2], v[3]);
+    }
+    st_128(p.out + off, o[0], o[1], o[2], o[3]);
+  }
+}
+
+namespace {
+
+std::mutex g_mu;
+std::map<std::tuple<const void*, int, size_t>, int> g_occ;   // (kernel, device, smem) -> blocks/SM
+std::map<int, int> g_sms;
+
+int grid_for(const void* fn, size_t smem, int64_t want) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto s = g_sms.find(dev);
+  if (s == g_sms.end()) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    s = g_sms.emplace(dev, n).first;
+  }
+  auto o = g_occ.find(std::make_tuple(fn, dev, smem));
+  if (o == g_occ.end()) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kThreads, smem) != cudaSuccess || nb < 1)
+      return -1;
+    o = g_occ.emplace(std::make_tuple(fn, dev, smem), nb).first;
+  }
+  const int64_t full = static_cast<int64_t>(o->second) * s->second;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, full)));
+}
+
+int launch(const void* fn, int grid, size_t smem, ptgq_stream_t stream, void** args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return PTGQ_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return PTGQ_ERR_CUDA;
+  return PTGQ_OK;
+}
+
+const void* per_token_fn(int dtype, bool wide) {
+  switch (dtype * 2 + (wide ? 1 : 0)) {
+    case 0: return reinterpret_cast<const void*>(&per_token_kernel<0, 8>);
+    case 1: return reinterpret_cast<const void*>(&per_token_kernel<0, 16>);
+    case 2: return reinterpret_cast<const void*>(&per_token_kernel<1, 8>);
+    case 3: return reinterpret_cast<const void*>(&per_token_kernel<1, 16>);
+    default: return reinterpret_cast<const void*>(&per_token_kernel<2, 16>);
+  }
+}
+
+}  // namespace
+}  // namespace ptgq
+
+using namespace ptgq;
+
+extern "C" int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens, int64_t hidden,
+                                    void* out_q, float* out_s, ptgq_stream_t stream) {
+  if (dtype != PTGQ_BF16 && dtype != PTGQ_FP16 && dtype != PTGQ_FP32) return PTGQ_ERR_DTYPE;
+  if (hidden <= 0 || hidden % 4 != 0) return PTGQ_ERR_HIDDEN;
+  if (num_tokens < 0) return PTGQ_ERR_SHAPE;
+  if (num_tokens > 0 && hidden > (int64_t(1) << 62) / num_tokens) return PTGQ_ERR_TOO_LARGE;
+  if (num_tokens == 0) return PTGQ_OK;
+  if (x == nullptr || out_q == nullptr || out_s == nullptr) return PTGQ_ERR_NULL;
+  const int esize = dtype == PTGQ_FP32 ? 4 : 2;
+  // 16-byte vectors when every row start is 16-byte aligned, else 8-byte vectors (16-bit
+  // rows whose length is a multiple of 4 but not of 8).
+  const bool wide = dtype == PTGQ_FP32 || hidden % 8 == 0;
+  const uintptr_t need = wide ? 16 : 8;
+  if (reinterpret_cast<uintptr_t>(x) % need != 0 || reinterpret_cast<uintptr_t>(out_q) % (wide && esize == 2 ? 8 : 4) != 0 ||
+      reinterpret_cast<uintptr_t>(out_s) % 4 != 0)
+    return PTGQ_ERR_ALIGN;
+  const void* fn = per_token_fn(dtype, wide);
+  const int grid = grid_for(fn, 0, (num_tokens + kWarps - 1) / kWarps);
+  if (grid < 0) return PTGQ_ERR_CUDA;
+  PerTokenParams p{x, static_cast<uint8_t*>(out_q), out_s, num_tokens, hidden};
+  void* args[] = {&p};
+  return launch(fn, grid, 0, stream, args);
+}
+
+extern "C" int ptgq_requant_per_tensor(const void* x, const float* x_scale, int64_t scale_stride_e,
+                                       int64_t scale_stride_m, int64_t scale_stride_g,
+                                       const int32_t* masked_m, const float* output_scale,
+                                       void* out, int64_t num_experts, int64_t m, int64_t k,
+                                       int group_size, ptgq_stream_t stream) {
+  if (group_size != 16 && group_size != 32 && group_size != 64 && group_size != 128)
+    return PTGQ_ERR_GROUP;
+  if (k <= 0 || k % group_size != 0) return PTGQ_ERR_HIDDEN;
+  if (num_experts < 0 || m < 0 || (masked_m != nullptr && num_experts > kMaxExperts))
+    return PTGQ_ERR_SHAPE;
+  if (num_experts > 0 && m > 0 &&
+      (num_experts * m > (int64_t(1) << 31) / (k / group_size) || m > (int64_t(1) << 31)))
+    return PTGQ_ERR_TOO_LARGE;
+  if (num_experts * m == 0) return PTGQ_OK;
+  if (x == nullptr || x_scale == nullptr || output_scale == nullptr || out == nullptr)
+    return PTGQ_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(x_scale) % 4 != 0 || reinterpret_cast<uintptr_t>(output_scale) % 4 != 0 ||
+      reinterpret_cast<uintptr_t>(masked_m) % 4 != 0)
+    return PTGQ_ERR_ALIGN;
+  RequantParams p{};
+  p.x = static_cast<const uint8_t*>(x);
+  p.x_scale = x_scale;
+  p.masked_m = masked_m;
+  p.output_scale = output_scale;
+  p.out = static_cast<uint8_t*>(out);
+  p.experts = num_experts;
+  p.m = m;
+  p.k = k;
+  p.se = scale_stride_e;
+  p.sm = scale_stride_m;
+  p.sg = scale_stride_g;
+  p.lg_log2 = static_cast<uint32_t>(__builtin_ctz(static_cast<unsigned>(group_size / 16)));
+  p.gpr = static_cast<uint32_t>(k / group_size);
+  p.gpr_magic = p.gpr == 1 ? 0xFFFFFFFFu : static_cast<uint32_t>((uint64_t(1) << 32) / p.gpr);
+  const size_t smem = masked_m ? static_cast<size_t>(num_experts + 1) * sizeof(int32_t) : 0;
+  const void* fn = reinterpret_cast<const void*>(&requant_kernel);
+  const int64_t groups = num_experts * m * (k / group_size);
+  const int64_t tasks = (groups * (group_size / 16) + 31) / 32;
+  const int grid = grid_for(fn, smem, (tasks + kWarps - 1) / kWarps);
+  if (grid < 0) return PTGQ_ERR_CUDA;
+  void* args[] = {&p};
+  return launch(fn, grid, smem, stream, args);
+}

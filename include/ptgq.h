@@ -43,8 +43,8 @@ extern "C" {
 
 typedef struct CUstream_st* ptgq_stream_t; /* the same type as cudaStream_t */
 
-/* Element type of x. */
-typedef enum { PTGQ_BF16 = 0, PTGQ_FP16 = 1 } ptgq_in_dtype;
+/* Element type of x.  PTGQ_FP32 is accepted by ptgq_per_token_quant only. */
+typedef enum { PTGQ_BF16 = 0, PTGQ_FP16 = 1, PTGQ_FP32 = 2 } ptgq_in_dtype;
 /* Element type of out_q: FP8 E4M3 ("fn", max 448) or int8. */
 typedef enum { PTGQ_E4M3 = 0, PTGQ_INT8 = 1 } ptgq_out_dtype;
 /* Scale format:
@@ -147,6 +147,58 @@ int ptgq_quant_ex(const void* x, int dtype, int64_t num_tokens_or_E, int64_t tok
 int ptgq_scale_elems(int64_t num_tokens_or_E, int64_t tokens_pad, int64_t hidden,
                      int group_size, int scale_fmt, int scale_layout, int masked,
                      int64_t* n_out);
+
+/*
+ * ptgq_per_token_quant -- per-token (whole-row) FP8 e4m3 quantization (sglang PR #34257,
+ * "Key source snippets": the per-token kernels and their host contract).
+ *
+ * For each row r < num_tokens of x [num_tokens, hidden]:
+ *   s   = max_i |x_i| / 448          (binary32 division; no eps floor)
+ *   inv = s == 0 ? 0 : 1 / s         (an all-zero row gets scale 0 and codes 0)
+ *   q_i = e4m3(clamp(x_i * inv, -448, 448)),   out_s[r] = s
+ * The multiplication by the reciprocal (not a division) is the page's definition.
+ *
+ *   x         device, row-major [num_tokens, hidden], dtype PTGQ_BF16, PTGQ_FP16 or
+ *             PTGQ_FP32; 16-byte aligned (8-byte suffices for 16-bit rows with
+ *             hidden % 8 != 0).
+ *   hidden    a positive multiple of 4.
+ *   out_q     device e4m3 codes, row-major with row length `hidden`; it may have more rows
+ *             than num_tokens (a padded output): rows past num_tokens are not touched.
+ *             8-byte aligned (4-byte when 16-bit rows have hidden % 8 != 0).
+ *   out_s     device float scales, one per row; entries past num_tokens are not touched.
+ * Returns PTGQ_OK or a negative status (checked before launching).
+ */
+int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens, int64_t hidden,
+                         void* out_q, float* out_s, ptgq_stream_t stream);
+
+/*
+ * ptgq_requant_per_tensor -- per-token-group FP8 to per-tensor FP8 requantization over the
+ * masked EP-MoE layout (sglang PR #35593, "Key source snippets": the requant kernel and
+ * test_masked_rows_and_k_tail).
+ *
+ * For every expert e < num_experts and row r < clamp(masked_m[e], 0, m) (all m rows when
+ * masked_m is NULL), and every column c < k:
+ *   out[e, r, c] = e4m3_satfinite((decode(x[e, r, c]) * x_scale[e, r, c / group_size])
+ *                                 * (1 / *output_scale))
+ * with binary32 products in that order and a saturating round-to-nearest-even conversion.
+ * Rows at or past masked_m[e] are neither read nor written.
+ *
+ *   x             device e4m3 codes [num_experts, m, k], row-major, 16-byte aligned.
+ *   x_scale       device float per-token-group scales; element (e, r, g) at
+ *                 e * scale_stride_e + r * scale_stride_m + g * scale_stride_g (strides in
+ *                 elements, e.g. the column-major [E, m, k/group] layout of the page:
+ *                 (m * k/group, 1, m)).  The caller guarantees every index is inside it.
+ *   masked_m      device int32[num_experts] live rows per expert, or NULL.
+ *   output_scale  device pointer to the one binary32 per-tensor output scale.
+ *   out           device e4m3 codes [num_experts, m, k], 16-byte aligned.
+ *   k             a multiple of group_size; group_size in {16, 32, 64, 128}.
+ * Returns PTGQ_OK or a negative status (checked before launching).
+ */
+int ptgq_requant_per_tensor(const void* x, const float* x_scale, int64_t scale_stride_e,
+                            int64_t scale_stride_m, int64_t scale_stride_g,
+                            const int32_t* masked_m, const float* output_scale, void* out,
+                            int64_t num_experts, int64_t m, int64_t k, int group_size,
+                            ptgq_stream_t stream);
 
 /* A static, human-readable description of a status code. */
 const char* ptgq_strerror(int status);

@@ -23,7 +23,8 @@ def L():
 
 def test_every_declared_function_is_exported(L):
     names = P.header_functions()
-    assert set(names) == {"ptgq_quant", "ptgq_quant_ex", "ptgq_scale_elems", "ptgq_strerror"}
+    assert set(names) == {"ptgq_quant", "ptgq_quant_ex", "ptgq_scale_elems", "ptgq_strerror",
+                          "ptgq_per_token_quant", "ptgq_requant_per_tensor"}
     for n in names:
         assert hasattr(L, n), n
 
@@ -97,3 +98,19 @@ def test_nothing_to_do_returns_ok_without_device(L):
     assert _call(L, x=0, q=0, s=0, n=0) == 0
     assert _call(L, x=0, q=0, s=0, n=0, mm=64, tokens_pad=0) == 0
     assert _call(L, x=0, q=0, s=0, n=0, mm=64, tokens_pad=16) == 0
+
+
+def test_per_token_and_requant_validation(L):
+    assert L.ptgq_per_token_quant(16, 3, 4, 64, 16, 16, None) == -2
+    assert L.ptgq_per_token_quant(16, 0, 4, 66, 16, 16, None) == -5
+    assert L.ptgq_per_token_quant(16, 0, -1, 64, 16, 16, None) == -6
+    assert L.ptgq_per_token_quant(0, 0, 4, 64, 16, 16, None) == -1
+    assert L.ptgq_per_token_quant(8, 0, 4, 64, 16, 16, None) == -7     # 16-byte rows need 16 B
+    assert L.ptgq_per_token_quant(0, 0, 0, 64, 0, 0, None) == 0        # nothing to do
+    rq = L.ptgq_requant_per_tensor
+    assert rq(16, 16, 1, 1, 1, None, 16, 16, 2, 4, 256, 100, None) == -4
+    assert rq(16, 16, 1, 1, 1, None, 16, 16, 2, 4, 200, 128, None) == -5
+    assert rq(16, 16, 1, 1, 1, None, 16, 16, -1, 4, 256, 128, None) == -6
+    assert rq(0, 16, 1, 1, 1, None, 16, 16, 2, 4, 256, 128, None) == -1
+    assert rq(8, 16, 1, 1, 1, None, 16, 16, 2, 4, 256, 128, None) == -7
+    assert rq(0, 0, 1, 1, 1, None, 0, 0, 0, 4, 256, 128, None) == 0
