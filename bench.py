@@ -264,6 +264,69 @@ class Workload:
                                masked=mm is not None)
 
 
+class PerTokenWorkload(Workload):
+    """Per-token (whole-row) FP8 quantization: x [T, hidden] -> e4m3 codes + one scale/row."""
+
+    def __init__(self, name, desc, tokens, hidden):
+        super().__init__(name, desc, None)
+        self.tokens, self.hidden = tokens, hidden
+
+    def inputs(self):
+        from fp8_token_group_gb300 import synth
+        import torch
+        return synth.normal((self.tokens, self.hidden), torch.bfloat16, seed=4), None
+
+    def live_rows(self, x, mm):
+        return x.shape[0]
+
+    def bytes_per_call(self, x, mm):
+        return x.shape[0] * x.shape[1] * 3 + x.shape[0] * 4
+
+    def alloc(self, P, xd, mm):
+        import torch
+        return (torch.empty(xd.shape, dtype=torch.float8_e4m3fn, device=xd.device),
+                torch.empty(xd.shape[0], dtype=torch.float32, device=xd.device))
+
+    def call(self, P, xd, q, s, mm=None):
+        P.per_token_quant(xd, q, s)
+
+
+class RequantWorkload(Workload):
+    """Per-token-group FP8 -> per-tensor FP8 requant over [E, M, K] with masked rows."""
+
+    def __init__(self, name, desc, experts, m, k, live_per_expert):
+        super().__init__(name, desc, None)
+        self.experts, self.m, self.k, self.live = experts, m, k, live_per_expert
+
+    def inputs(self):
+        import torch
+        g = torch.Generator().manual_seed(6)
+        x = torch.randint(-8, 9, (self.experts, self.m, self.k), generator=g).float()
+        codes = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        mm = torch.full((self.experts,), self.live, dtype=torch.int32)
+        return codes, mm
+
+    def live_rows(self, x, mm):
+        return int(mm.clamp(0, x.shape[1]).sum())
+
+    def bytes_per_call(self, x, mm):
+        live = self.live_rows(x, mm)
+        return live * self.k * 2 + live * (self.k // 128) * 4
+
+    def alloc(self, P, xd, mm):
+        import torch
+        E, M, K = xd.shape
+        g = torch.Generator(device="cpu").manual_seed(7)
+        exps = torch.randint(-1, 2, (E, K // 128, M), generator=g).float()
+        xs = torch.pow(2.0, exps).to(xd.device).permute(0, 2, 1)     # column-major [E, M, K/128]
+        out = torch.empty_like(xd)
+        self._scale = torch.tensor([2.0], dtype=torch.float32, device=xd.device)
+        return out, xs
+
+    def call(self, P, xd, out, xs, mm=None):
+        P.requant_per_tensor(xd, xs, mm, self._scale, out, group_size=128)
+
+
 def workloads():
     from fp8_token_group_gb300 import synth
     import torch
@@ -280,6 +343,11 @@ def workloads():
         "sweep_big": Workload("sweep_big", "flat bf16 [32768,7168] N(0,1), G=128, e4m3, fp32 "
                               "row-major", lambda: synth.normal((32768, 7168), torch.bfloat16,
                                                                 seed=1)),
+        "per_token": PerTokenWorkload("per_token", "per-token FP8 quant, bf16 [4096,4096] "
+                                      "N(0,1) -> e4m3 + fp32 scale per row", 4096, 4096),
+        "requant": RequantWorkload("requant", "per-token-group -> per-tensor FP8 requant, e4m3 "
+                                   "[8 experts, 1024, 3584], 128 live rows per expert (1024 "
+                                   "live rows), column-major group scales", 8, 1024, 3584, 128),
     }
 
 
@@ -338,34 +406,60 @@ def time_graph(P, wl, sets, steps: int, warmup: int, world: int, sampler=None):
 
 
 def time_e2e(P, wl, x_cpu, mm_cpu, steps: int, device):
-    """Public API with host buffers: per step H2D of x (pinned), quantize, D2H of q and s."""
+    """Public API with host buffers.  Every step copies its input from pinned host memory to
+    the device, quantizes it, and copies codes and scales back to pinned host memory.
+    Steps are double-buffered on three streams (H2D, compute, D2H) so the copy of step i+1
+    overlaps the quantization and read-back of step i."""
     import torch
     xh = x_cpu.pin_memory()
-    xd = torch.empty_like(xh, device=device)
     mm = None if mm_cpu is None else mm_cpu.to(device)
-    q, s = wl.alloc(P, xd, mm)
-    qh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-    sh = torch.empty(s.shape, dtype=s.dtype).pin_memory()
+    bufs = []
+    for _ in range(2):
+        xd = torch.empty_like(xh, device=device)
+        q, s = wl.alloc(P, xd, mm)
+        qh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        sh = torch.empty(s.shape, dtype=s.dtype).pin_memory()
+        bufs.append((xd, q, s, qh, sh))
+    h2d, comp, d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    copied = [ev(), ev()]     # input of buffer b is on the device
+    quantized = [ev(), ev()]  # outputs of buffer b are ready
+    returned = [ev(), ev()]   # outputs of buffer b are back on the host
+    consumed = [ev(), ev()]   # buffer b's input was consumed by its quantization
+    for e in returned + consumed:
+        e.record(torch.cuda.current_stream())
 
-    def step():
-        xd.copy_(xh, non_blocking=True)
-        wl.call(P, xd, q, s, mm)
-        qh.copy_(q, non_blocking=True)
-        sh.copy_(s, non_blocking=True)
+    def step(i):
+        b = i % 2
+        xd, q, s, qh, sh = bufs[b]
+        h2d.wait_event(consumed[b])
+        with torch.cuda.stream(h2d):
+            xd.copy_(xh, non_blocking=True)
+            copied[b].record(h2d)
+        comp.wait_event(copied[b])
+        comp.wait_event(returned[b])
+        with torch.cuda.stream(comp):
+            wl.call(P, xd, q, s, mm)
+            consumed[b].record(comp)
+            quantized[b].record(comp)
+        d2h.wait_event(quantized[b])
+        with torch.cuda.stream(d2h):
+            qh.copy_(q, non_blocking=True)
+            sh.copy_(s, non_blocking=True)
+            returned[b].record(d2h)
 
-    for _ in range(3):
-        step()
+    for i in range(4):
+        step(i)
     torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        step()
-    end.record()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(i)
     torch.cuda.synchronize()
-    el = start.elapsed_time(end) / 1e3
-    h2d = xh.numel() * xh.element_size()
-    d2h = qh.numel() * qh.element_size() + sh.numel() * sh.element_size()
-    return el, h2d, d2h
+    el = time.perf_counter() - t0
+    h2d_b = xh.numel() * xh.element_size()
+    qh, sh = bufs[0][3], bufs[0][4]
+    d2h_b = qh.numel() * qh.element_size() + sh.numel() * sh.element_size()
+    return el, h2d_b, d2h_b
 
 
 def measure_device(P, wl, device, steps: int) -> dict:
@@ -441,8 +535,9 @@ def run_ours(args, world, rank, local):
             "gpu_launches": calls,
             "e2e": {"value": round(world * e2e_steps * bpc / e2e_el / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "pinned host x -> device, fp8_token_group_gb300.quant, codes and "
-                            "scales -> pinned host, per step"},
+                    "path": "per step: pinned host x -> device, fp8_token_group_gb300.quant, "
+                            "codes and scales -> pinned host; double-buffered on H2D/compute/"
+                            "D2H streams, wall clock over all steps"},
             "cpu_baseline": base,
             "other_workloads": others,
         }
@@ -461,7 +556,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat_outliers",
                     choices=["flat_outliers", "flat_small", "silu_flat", "masked_silu",
-                             "sweep_big"], help="workload of the JSON line (default: the "
+                             "sweep_big", "per_token", "requant"], help="workload of the JSON line (default: the "
                     "benchmarked flat_outliers)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")

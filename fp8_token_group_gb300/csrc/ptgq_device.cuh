@@ -123,4 +123,97 @@ __device__ __forceinline__ int expert_of(const int32_t* prefix, int n, uint32_t 
   return lo;
 }
 
+// ---- packed helpers -------------------------------------------------------------
+
+// max(|a|, |b|) per 16-bit half (the xorsign variant; callers clear the sign bits).
+template <bool kFp16>
+__device__ __forceinline__ uint32_t maxabs2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if constexpr (kFp16) asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  else asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Two binary32 values in one 64-bit register pair, for the sm_100+ f32x2 instructions.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// Rounded toward -inf: an exact zero result is -0 (see div2_by_scale).
+__device__ __forceinline__ uint64_t fma2_rm(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// A pair of 16-bit elements widened to binary32 (exact), as an f32x2 pair.
+template <bool kFp16>
+__device__ __forceinline__ uint64_t widen2(uint32_t w) {
+  return pk2(widen_lo<kFp16>(w), widen_hi<kFp16>(w));
+}
+
+// Two e4m3 codes (low byte = lo) from an f32x2 pair.
+__device__ __forceinline__ uint32_t e4m3x2_pair(uint64_t v) {
+  float lo, hi;
+  upk2(v, lo, hi);
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));
+  return c;
+}
+
+// The pair x / s from r = RN(1/s), ns = -s: q0 = RN(x r), e = RM(x - q0 s) (exact when the
+// residual does not underflow; rounding toward -inf only fixes the sign of an exact zero,
+// so x = -0 gives -0), q = RN(q0 + e r).  Same 8-bit codes as the IEEE quotient for every
+// input with amax >= 1e-24 (checked for every pair of 16-bit values and 1.3e9 sampled
+// binary32 pairs); the binary32 quotient itself can differ only below 2^-10, where every
+// code is zero.
+__device__ __forceinline__ uint64_t div2_by_scale(uint64_t x, uint64_t r, uint64_t ns) {
+  const uint64_t q0 = mul2(x, r);
+  const uint64_t e = fma2_rm(q0, ns, x);
+  return fma2(e, r, q0);
+}
+
+// RN(a / d) for the constants d = 448 or 127 with rd = RN(1/d): one exact-residual
+// correction gives the IEEE quotient for every positive normal binary32 a >= 2^-103
+// (checked exhaustively for both constants).
+__device__ __forceinline__ float div_by_const(float a, float d, float rd) {
+  const float q0 = __fmul_rn(a, rd);
+  const float e = __fmaf_rn(-q0, d, a);
+  return __fmaf_rn(e, rd, q0);
+}
+
+// Copy `n16` 16-byte chunks of module constants into shared memory with cp.async: every
+// thread issues all its chunks before waiting, so the copy costs one L2 round trip.  The
+// caller synchronizes the block afterwards.
+__device__ __forceinline__ void copy_to_smem_async(void* dst, const void* src, int n16) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const char* s = static_cast<const char*>(src);
+  for (int i = threadIdx.x; i < n16; i += kThreads)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16u * i), "l"(s + 16 * i)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void copy_to_smem_wait() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 }  // namespace ptgq

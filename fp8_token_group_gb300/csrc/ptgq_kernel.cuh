@@ -31,8 +31,8 @@
 
 namespace ptgq {
 
-constexpr int kExpIntWords = 2 * (PTGQ_EXP_INT_MAX - PTGQ_EXP_INT_MIN + 1);
-constexpr int kExpFracWords = 2 * (PTGQ_EXP_FRAC_JMAX - PTGQ_EXP_FRAC_JMIN + 1);
+constexpr int kExpIntWords = PTGQ_EXP_INT_WORDS;     // (hi, lo) pairs, padded to 16 bytes
+constexpr int kExpFracWords = PTGQ_EXP_FRAC_WORDS;
 constexpr int kSiluBf16Words = 2 * PTGQ_SILU_BF16_SPAN;
 
 template <bool kFp16, bool kSilu>
@@ -43,37 +43,42 @@ struct SmemTables {
   static constexpr int bytes = (words * 4 + 15) / 16 * 16;
 };
 
-// One lane's share of a warp task.
+// What finish() needs of one lane's share of a warp task (issue() computes it).
 struct Slot {
-  const uint16_t* src;   // first input element (gate half with silu)
-  uint8_t* dst;          // first code byte
-  int64_t s_base;        // scale block base (elements)
-  uint32_t row;          // row within the block
-  uint32_t g;            // group within the row
-  uint32_t c;            // unit within the row
+  uint8_t* dst;          // first code byte of the lane's 16 elements
+  int64_t sidx;          // scale element this lane stores (group or unit leader)
   bool unit_valid;       // the unit exists
   bool valid;            // the unit exists and this lane's group is inside the row
 };
 
+// Tuning parameters (compile-time): tasks per warp batch without silu (with silu: 1),
+// whether the next batch's loads are issued before the current batch is computed, and the
+// CTAs per SM the register budget is sized for.
+#ifndef PTGQ_TASK_BATCH
+#define PTGQ_TASK_BATCH 2
+#endif
+#ifndef PTGQ_PIPELINE
+#define PTGQ_PIPELINE 1
+#endif
+#ifndef PTGQ_MIN_BLOCKS
+#define PTGQ_MIN_BLOCKS 3
+#endif
+template <bool kSilu> struct Batch { static constexpr int n = kSilu ? 1 : PTGQ_TASK_BATCH; };
+
 template <bool kFp16, bool kInt8, bool kPow2, bool kSilu>
-__global__ void __launch_bounds__(kThreads) quant_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   using Tab = SmemTables<kFp16, kSilu>;
+  constexpr int kB = Batch<kSilu>::n;
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Tab::bytes);
 
-  // Module constants first: they do not depend on the previous grid.
+  // Module constants first (asynchronously): they do not depend on the previous grid.
   if constexpr (kSilu) {
-    uint4* dst = reinterpret_cast<uint4*>(smem);
     if constexpr (kFp16) {
-      const uint32_t* a = kExpIntHL;
-      const uint32_t* b = kExpFracHL;
-      uint32_t* d32 = reinterpret_cast<uint32_t*>(smem);
-      for (int i = threadIdx.x; i < kExpIntWords; i += kThreads) d32[i] = a[i];
-      for (int i = threadIdx.x; i < kExpFracWords; i += kThreads) d32[kExpIntWords + i] = b[i];
-      (void)dst;
+      copy_to_smem_async(smem, kExpIntHL, kExpIntWords / 4);
+      copy_to_smem_async(smem + 4 * kExpIntWords, kExpFracHL, kExpFracWords / 4);
     } else {
-      const uint4* src = reinterpret_cast<const uint4*>(kSiluBf16);
-      for (int i = threadIdx.x; i < kSiluBf16Words / 4; i += kThreads) dst[i] = src[i];
+      copy_to_smem_async(smem, kSiluBf16, kSiluBf16Words / 4);
     }
   }
 
@@ -81,12 +86,10 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const Params p) {
   griddep_launch_dependents();
 
   const bool masked = p.masked_m != nullptr;
-  uint32_t total_units = p.units_flat;
-  if (masked) {
-    masked_prefix(p.masked_m, p.n, p.rows, prefix);
-  }
+  if (masked) masked_prefix(p.masked_m, p.n, p.rows, prefix);
+  if constexpr (kSilu) copy_to_smem_wait();
   __syncthreads();
-  if (masked) total_units = static_cast<uint32_t>(prefix[p.n]) * p.upr;
+  const uint32_t total_units = masked ? static_cast<uint32_t>(prefix[p.n]) * p.upr : p.units_flat;
 
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t lu_log2 = p.lg_log2 + p.ug_log2;            // log2(lanes per unit)
@@ -94,45 +97,52 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const Params p) {
   const uint32_t lg = 1u << p.lg_log2;
   const uint32_t lu = 1u << lu_log2;
   const uint32_t local = lane & (lu - 1u);
+  const uint32_t lane_unit = lane >> lu_log2;                // unit within the warp task
   const uint32_t gj = local >> p.lg_log2;                    // group within the unit
   const uint32_t kk = local & (lg - 1u);                     // lane within the group
-  const uint32_t gmask = (lg == 32u ? 0xFFFFFFFFu : ((1u << lg) - 1u)) << (lane & ~(lg - 1u));
+  const uint32_t gmask = ((1u << lg) - 1u) << (lane & ~(lg - 1u));
   const uint32_t umask = (lu == 32u ? 0xFFFFFFFFu : ((1u << lu) - 1u)) << (lane & ~(lu - 1u));
   const uint32_t G = 16u << p.lg_log2;
   const uint32_t total_tasks = (total_units + (1u << upw_log2) - 1u) >> upw_log2;
   const uint32_t stride = gridDim.x * kWarps;
-  const uint32_t first = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
   uint8_t* __restrict__ q = static_cast<uint8_t*>(p.q);
   const float* silu_tab = reinterpret_cast<const float*>(smem);
+  const float rfmax = p.fmax == 448.0f ? (1.0f / 448.0f) : (1.0f / 127.0f);
+  const bool packed = p.scale_fmt == 1;
 
-  auto prep = [&](uint32_t t) {
-    Slot sl;
-    const uint32_t u = (t << upw_log2) + (lane >> lu_log2);
-    sl.unit_valid = t < total_tasks && u < total_units;
-    const uint32_t uu = sl.unit_valid ? u : 0u;
-    const uint32_t R = udiv(uu, p.upr, p.upr_magic);
-    sl.c = uu - R * p.upr;
-    sl.g = (sl.c << p.ug_log2) + gj;
-    sl.valid = sl.unit_valid && sl.g < p.ng;
-    int64_t blk = 0;
-    uint32_t r = R;
+  // Address the lane's 16 elements of task t and start its loads.  Lanes past the end
+  // (or in the unused groups of a partial unit) read a valid address of the last unit
+  // and are masked off later, so no load is ever predicated away.
+  auto issue = [&](uint32_t t, Slot& sl, Raw16& a, Raw16& b) {
+    const uint32_t u0 = (t << upw_log2) + lane_unit;
+    sl.unit_valid = u0 < total_units;
+    const uint32_t u = sl.unit_valid ? u0 : total_units - 1u;
+    const uint32_t R = udiv(u, p.upr, p.upr_magic);
+    const uint32_t c = u - R * p.upr;
+    const uint32_t g = (c << p.ug_log2) + gj;
+    sl.valid = sl.unit_valid && g < p.ng;
+    const uint32_t ge = g < p.ng ? g : p.ng - 1u;
+    int64_t grow = R, sbase = 0;
+    uint32_t row = R;
     if (masked) {
       const int e = expert_of(prefix, static_cast<int>(p.n), R);
-      r = R - static_cast<uint32_t>(prefix[e]);
-      blk = e;
+      row = R - static_cast<uint32_t>(prefix[e]);
+      grow = static_cast<int64_t>(e) * p.rows + row;
+      sbase = static_cast<int64_t>(e) * p.s_per_block;
     }
-    sl.row = r;
-    const int64_t grow = blk * p.rows + r;
-    const int64_t col = static_cast<int64_t>(sl.g) * G + kk * 16u;
-    sl.src = x + grow * p.in_row + col;
+    const int64_t col = static_cast<int64_t>(ge) * G + kk * 16u;
+    const uint16_t* src = x + grow * p.in_row + col;
+    ld_stream_256(a, src);
+    if constexpr (kSilu) ld_stream_256(b, src + p.hidden);
     sl.dst = q + grow * p.hidden + col;
-    sl.s_base = blk * p.s_per_block;
-    return sl;
+    const uint32_t sc = packed ? c : g;
+    sl.sidx = sbase + (p.col_major ? static_cast<int64_t>(sc) * p.s_mn_pad + row
+                                   : static_cast<int64_t>(row) * p.s_ncol + sc);
   };
 
   auto finish = [&](const Slot& sl, const Raw16& a, const Raw16& b) {
-    float v[16];
+    uint64_t v[8];                  // the 16 values as f32x2 pairs
     uint32_t amax_bits;
     if constexpr (kSilu) {
       amax_bits = 0u;
@@ -148,85 +158,97 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const Params p) {
           s0 = silu_bf16(a.w[i] & 0xFFFFu, silu_tab, PTGQ_SILU_BF16_FIELD_LO, PTGQ_SILU_BF16_SPAN);
           s1 = silu_bf16(a.w[i] >> 16, silu_tab, PTGQ_SILU_BF16_FIELD_LO, PTGQ_SILU_BF16_SPAN);
         }
-        v[2 * i] = __fmul_rn(s0, widen_lo<kFp16>(b.w[i]));
-        v[2 * i + 1] = __fmul_rn(s1, widen_hi<kFp16>(b.w[i]));
-        amax_bits = max(amax_bits, f2u(v[2 * i]) & 0x7FFFFFFFu);
-        amax_bits = max(amax_bits, f2u(v[2 * i + 1]) & 0x7FFFFFFFu);
+        v[i] = mul2(pk2(s0, s1), widen2<kFp16>(b.w[i]));
+        float y0, y1;
+        upk2(v[i], y0, y1);
+        amax_bits = max(amax_bits, max(f2u(y0) & 0x7FFFFFFFu, f2u(y1) & 0x7FFFFFFFu));
       }
     } else {
-      // |x| of 16-bit floats orders like the unsigned bit patterns without the sign.
-      uint32_t m = 0u;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        m = __vmaxu2(m, a.w[i] & 0x7FFF7FFFu);
-        v[2 * i] = widen_lo<kFp16>(a.w[i]);
-        v[2 * i + 1] = widen_hi<kFp16>(a.w[i]);
-      }
+      uint32_t m01 = maxabs2<kFp16>(a.w[0], a.w[1]), m23 = maxabs2<kFp16>(a.w[2], a.w[3]);
+      uint32_t m45 = maxabs2<kFp16>(a.w[4], a.w[5]), m67 = maxabs2<kFp16>(a.w[6], a.w[7]);
+      const uint32_t m = maxabs2<kFp16>(maxabs2<kFp16>(m01, m23), maxabs2<kFp16>(m45, m67)) &
+                         0x7FFF7FFFu;
       const uint32_t hm = max(m & 0xFFFFu, m >> 16);
       amax_bits = f2u(widen_lo<kFp16>(hm));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = widen2<kFp16>(a.w[i]);
       (void)b;
     }
     amax_bits = redux_max(sl.valid ? amax_bits : 0u, gmask);
     const float amax = fmaxf(u2f(amax_bits), p.eps);
-    float s = __fdiv_rn(amax, p.fmax);
+    float s = div_by_const(amax, p.fmax, rfmax);
     uint32_t e = 0u;
-    float y[16];
+    uint64_t y[8];
     if constexpr (kPow2) {
       if (p.scale_floor) s = fmaxf(s, 1e-10f);
       e = ue8m0_exponent(s);
       const float inv = ue8m0_inverse(e);
+      const uint64_t inv2 = pk2(inv, inv);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(v[i], inv);
+      for (int i = 0; i < 8; ++i) y[i] = mul2(v[i], inv2);
     } else {
       const float r = __frcp_rn(s);
+      const uint64_t r2 = pk2(r, r), ns2 = pk2(-s, -s);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = div_by_scale(v[i], s, r);
+      for (int i = 0; i < 8; ++i) y[i] = div2_by_scale(v[i], r2, ns2);
     }
     uint32_t o[4];
+    if constexpr (kInt8) {
+      // + 1.5 * 2^23 rounds |y| <= 127 to the nearest integer (ties to even) in the low byte
+      const uint64_t magic = pk2(12582912.0f, 12582912.0f);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if constexpr (kInt8) o[i] = s8x4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-      else o[i] = e4m3x4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+      for (int i = 0; i < 4; ++i) {
+        float a0, a1, b0, b1;
+        upk2(add2(y[2 * i], magic), a0, a1);
+        upk2(add2(y[2 * i + 1], magic), b0, b1);
+        o[i] = __byte_perm(__byte_perm(f2u(a0), f2u(a1), 0x0040u),
+                           __byte_perm(f2u(b0), f2u(b1), 0x0040u), 0x5410u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = e4m3x2_pair(y[2 * i]) | (e4m3x2_pair(y[2 * i + 1]) << 16);
     }
     if (sl.valid) st_128(sl.dst, o[0], o[1], o[2], o[3]);
 
-    // scales
-    if (p.scale_fmt == 1) {
+    if (packed) {
       const uint32_t word = redux_or(sl.valid && kk == 0u ? (e << (8u * gj)) : 0u, umask);
-      if (sl.unit_valid && local == 0u) {
-        const int64_t idx = p.col_major ? sl.s_base + static_cast<int64_t>(sl.c) * p.s_mn_pad + sl.row
-                                        : sl.s_base + static_cast<int64_t>(sl.row) * p.s_ncol + sl.c;
-        static_cast<uint32_t*>(p.s)[idx] = word;
-      }
+      if (sl.unit_valid && local == 0u) static_cast<uint32_t*>(p.s)[sl.sidx] = word;
     } else if (sl.valid && kk == 0u) {
-      const float sv = p.scale_fmt == 0 ? s : u2f(e << 23);
-      const int64_t idx = p.col_major ? sl.s_base + static_cast<int64_t>(sl.g) * p.s_mn_pad + sl.row
-                                      : sl.s_base + static_cast<int64_t>(sl.row) * p.s_ncol + sl.g;
-      static_cast<float*>(p.s)[idx] = sv;
+      static_cast<float*>(p.s)[sl.sidx] = p.scale_fmt == 0 ? s : u2f(e << 23);
     }
   };
 
-  // Two tasks in flight per warp: both loads are issued before either is used.
-  for (uint32_t t = first; t < total_tasks; t += 2u * stride) {
-    const Slot s0 = prep(t);
-    const Slot s1 = prep(t + stride);
-    Raw16 a0, a1, b0, b1;
-    if (s0.valid) ld_stream_256(a0, s0.src);
-    if (s1.valid) ld_stream_256(a1, s1.src);
-    if constexpr (kSilu) {
-      if (s0.valid) ld_stream_256(b0, s0.src + p.hidden);
-      if (s1.valid) ld_stream_256(b1, s1.src + p.hidden);
-    }
-    if (!s0.valid) {
+  // Software pipeline: the next batch's loads are in flight while this batch computes.
+  if (total_units > 0u && !PTGQ_PIPELINE) {
+    for (uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_tasks; t += kB * stride) {
+      Slot cur[kB];
+      Raw16 ca[kB], cb[kB];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a0.w[i] = b0.w[i] = 0u;
-    }
-    if (!s1.valid) {
+      for (int i = 0; i < kB; ++i) issue(t + i * stride, cur[i], ca[i], cb[i]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a1.w[i] = b1.w[i] = 0u;
+      for (int i = 0; i < kB; ++i) finish(cur[i], ca[i], cb[i]);
     }
-    finish(s0, a0, b0);
-    finish(s1, a1, b1);
+  } else if (total_units > 0u) {
+    uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    Slot cur[kB];
+    Raw16 ca[kB], cb[kB];
+#pragma unroll
+    for (int i = 0; i < kB; ++i) issue(t + i * stride, cur[i], ca[i], cb[i]);
+    while (t < total_tasks) {
+      Slot nxt[kB];
+      Raw16 na[kB], nb[kB];
+#pragma unroll
+      for (int i = 0; i < kB; ++i) issue(t + (kB + i) * stride, nxt[i], na[i], nb[i]);
+#pragma unroll
+      for (int i = 0; i < kB; ++i) finish(cur[i], ca[i], cb[i]);
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        cur[i] = nxt[i];
+        ca[i] = na[i];
+        cb[i] = nb[i];
+      }
+      t += kB * stride;
+    }
   }
 
   // Flat scheduler: zero the padding rows of out_q and of the scales.

@@ -143,17 +143,4 @@ PTGQ_HD uint32_t ue8m0_exponent(float s) {
 // 2^(127 - e), the exact reciprocal of the UE8M0 scale 2^(e - 127) (e <= 253).
 PTGQ_HD float ue8m0_inverse(uint32_t e) { return u2f((254u - e) << 23); }
 
-// Quotient x / s from the correctly rounded reciprocal r = RN(1/s): q0 = RN(x r),
-// then one exact-residual correction q = RN(q0 + RN(x - q0 s) r).  For every
-// input this gives the same 8-bit code as the IEEE quotient (verified for every
-// pair of 16-bit values and sampled binary32 values, amax >= 1e-24); it can
-// differ from the IEEE quotient only below 2^-10, where every code is zero.  The
-// sign of x is restored because x = -0 would otherwise give +0.
-PTGQ_HD float div_by_scale(float x, float s, float r) {
-  const float q0 = x * r;
-  const float e = fmaf(q0, -s, x);
-  const float q = fmaf(e, r, q0);
-  return u2f(f2u(q) | (f2u(x) & 0x80000000u));
-}
-
 }  // namespace ptgq
