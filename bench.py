@@ -38,7 +38,7 @@ WORKLOAD = "flat bf16 x[4096,7168] N(0,1)+0.1% outliers x100+1% zero groups, G=1
 T, H, G = 4096, 7168, 128
 GRAPH_CALLS = 400                      # calls captured per CUDA graph
 KERNEL_SOURCES = ["ptgq_kernel.cuh", "ptgq_math.cuh", "ptgq_api.cu", "ptgq_internal.h",
-                  "ptgq_inst_bf16.cu", "silu_tables.inc"]
+                  "ptgq_inst_bf16_flat.cu", "ptgq_device.cuh", "silu_tables.inc"]
 
 
 def algorithmic_bytes(tokens: int = T, hidden: int = H, group: int = G) -> int:

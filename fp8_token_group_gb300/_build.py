@@ -10,7 +10,8 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libptgq.so")
-SOURCES = ["ptgq_api.cu", "ptgq_inst_bf16.cu", "ptgq_inst_fp16.cu", "ptgq_next.cu"]
+SOURCES = ["ptgq_api.cu", "ptgq_inst_bf16_flat.cu", "ptgq_inst_bf16_masked.cu",
+           "ptgq_inst_fp16_flat.cu", "ptgq_inst_fp16_masked.cu", "ptgq_next.cu"]
 HEADERS = ["ptgq_internal.h", "ptgq_kernel.cuh", "ptgq_device.cuh", "ptgq_math.cuh",
            "silu_tables.inc"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

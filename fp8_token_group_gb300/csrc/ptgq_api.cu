@@ -17,13 +17,19 @@
 
 namespace ptgq {
 
-const void* kernel_for_bf16(int int8, int pow2, int silu);
-const void* kernel_for_fp16(int int8, int pow2, int silu);
+const void* kernel_for_bf16_flat(int int8, int fmt, int silu);
+const void* kernel_for_bf16_masked(int int8, int fmt, int silu);
+const void* kernel_for_fp16_flat(int int8, int fmt, int silu);
+const void* kernel_for_fp16_masked(int int8, int fmt, int silu);
 int table_bytes_bf16(int silu);
 int table_bytes_fp16(int silu);
 
 const void* kernel_for(const KernelKey& k) {
-  return k.fp16 ? kernel_for_fp16(k.int8, k.pow2, k.silu) : kernel_for_bf16(k.int8, k.pow2, k.silu);
+  if (k.fp16)
+    return k.masked ? kernel_for_fp16_masked(k.int8, k.fmt, k.silu)
+                    : kernel_for_fp16_flat(k.int8, k.fmt, k.silu);
+  return k.masked ? kernel_for_bf16_masked(k.int8, k.fmt, k.silu)
+                  : kernel_for_bf16_flat(k.int8, k.fmt, k.silu);
 }
 
 size_t dynamic_smem_bytes(const KernelKey& k, int64_t experts) {
@@ -182,15 +188,14 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   p.s_per_block = g.per_block;
   p.eps = eps;
   p.fmax = out_dtype == PTGQ_E4M3 ? 448.0f : 127.0f;
-  p.scale_floor = (flags & PTGQ_FLAG_UE8M0_SCALE_FLOOR) ? 1 : 0;
+  p.scale_floor = (flags & PTGQ_FLAG_UE8M0_SCALE_FLOOR) ? 1e-10f : 0.0f;
   if (!masked) {
     p.zero_q_begin = n * hidden;
     p.zero_q_end = g.rows * hidden;
     p.zero_s_rows = (scale_layout == PTGQ_ROW_MAJOR ? g.rows : g.mn_pad) - n;
   }
 
-  const KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, scale_fmt != PTGQ_SCALE_FP32,
-                      fuse_silu};
+  const KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, scale_fmt, fuse_silu, masked};
   const void* fn = kernel_for(key);
   const size_t smem = dynamic_smem_bytes(key, masked ? n : 0);
   int dev = 0;

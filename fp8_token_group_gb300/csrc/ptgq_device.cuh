@@ -30,14 +30,27 @@ __device__ __forceinline__ void st_128(void* p, uint32_t a, uint32_t b, uint32_t
                : "memory");
 }
 
+// Predicated stores: the predicate guards the instruction itself, so no branch (and no
+// reconvergence) is generated around them.
+__device__ __forceinline__ void st_128_if(bool pred, void* p, uint32_t a, uint32_t b, uint32_t c,
+                                          uint32_t d) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q st.global.v4.b32 [%0], {%1,%2,%3,%4};\n\t}" ::"l"(p),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+__device__ __forceinline__ void st_32_if(bool pred, void* p, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.b32 [%0], %1;\n\t}" ::"l"(p),
+      "r"(v), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
+// Warp-wide unsigned max (callers pass the full mask).
 __device__ __forceinline__ uint32_t redux_max(uint32_t v, uint32_t mask) {
   uint32_t r;
   asm volatile("redux.sync.max.u32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(mask));
-  return r;
-}
-__device__ __forceinline__ uint32_t redux_or(uint32_t v, uint32_t mask) {
-  uint32_t r;
-  asm volatile("redux.sync.or.b32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(mask));
   return r;
 }
 
@@ -214,6 +227,26 @@ __device__ __forceinline__ void copy_to_smem_async(void* dst, const void* src, i
 }
 __device__ __forceinline__ void copy_to_smem_wait() {
   asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Max over the `lg` lanes of a group (lg a power of two <= 8, groups aligned to lg lanes);
+// every lane of the group receives it.  Fixed-width butterfly with full-warp shuffles and
+// predicated selects, so it compiles to straight-line code for any lg.
+__device__ __forceinline__ uint32_t group_max(uint32_t v, uint32_t lg) {
+#pragma unroll
+  for (uint32_t o = 1; o < 8; o <<= 1) {
+    const uint32_t w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = o < lg ? max(v, w) : v;
+  }
+  return v;
+}
+
+// OR of the four groups of a unit (4*lg lanes, aligned): lanes exchange with the lanes of
+// the same rank in groups j^1 and j^2, so every lane receives the OR of all four.
+__device__ __forceinline__ uint32_t unit_or(uint32_t v, uint32_t lg) {
+  v |= __shfl_xor_sync(0xFFFFFFFFu, v, lg);
+  v |= __shfl_xor_sync(0xFFFFFFFFu, v, 2u * lg);
+  return v;
 }
 
 }  // namespace ptgq

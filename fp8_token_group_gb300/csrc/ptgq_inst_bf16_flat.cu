@@ -1,0 +1,27 @@
+// ptgq_inst_bf16_flat.cu -- kernel instances for bf16 input, flat scheduler (one translation
+// unit per input type and scheduler, so the instances compile in parallel).
+#include "ptgq_kernel.cuh"
+
+namespace ptgq {
+
+const void* kernel_for_bf16_flat(int int8, int fmt, int silu) {
+  static const void* const table[12] = {
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 0, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 0, true, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 1, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 1, true, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 2, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 2, true, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 0, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 0, true, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 1, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 1, true, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 2, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 2, true, false>),
+  };
+  return table[(int8 ? 6 : 0) + fmt * 2 + (silu ? 1 : 0)];
+}
+
+int table_bytes_bf16(int silu) { return silu ? SmemTables<false, true>::bytes : 0; }
+
+}  // namespace ptgq

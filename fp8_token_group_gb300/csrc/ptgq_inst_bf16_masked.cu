@@ -1,0 +1,25 @@
+// ptgq_inst_bf16_masked.cu -- kernel instances for bf16 input, masked scheduler (one translation
+// unit per input type and scheduler, so the instances compile in parallel).
+#include "ptgq_kernel.cuh"
+
+namespace ptgq {
+
+const void* kernel_for_bf16_masked(int int8, int fmt, int silu) {
+  static const void* const table[12] = {
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 0, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 0, true, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 1, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 1, true, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 2, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 2, true, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 0, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 0, true, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 1, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 1, true, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 2, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 2, true, true>),
+  };
+  return table[(int8 ? 6 : 0) + fmt * 2 + (silu ? 1 : 0)];
+}
+
+}  // namespace ptgq

@@ -39,19 +39,21 @@ struct Params {
   int64_t s_per_block;       // scale elements per block (per expert)
   float eps;                 // amax floor
   float fmax;                // 448 (e4m3) or 127 (int8)
-  int32_t scale_floor;       // vLLM UE8M0 semantics: s = max(s, 1e-10) before rounding
+  float scale_floor;         // UE8M0 only: s = max(s, scale_floor); 1e-10 for the vLLM
+                             // semantics, else 0 (a no-op since s > 0)
   // Flat zero-fill of padding (rows [T, rows) of q; scale rows past T).
   int64_t zero_q_begin;      // byte offsets into q, multiples of 16
   int64_t zero_q_end;
   int64_t zero_s_rows;       // scale rows to zero per column: [T, T + zero_s_rows)
 };
 
-// One kernel instance per (input type, output type, scale arithmetic, silu).
+// One kernel instance per (input type, output type, scale arithmetic, silu, scheduler).
 struct KernelKey {
   int fp16;       // input is fp16 (else bf16)
   int int8;       // output is int8 (else e4m3)
-  int pow2;       // UE8M0 scale (multiply by an exact power of two) vs fp32 division
+  int fmt;        // scale format: 0 fp32, 1 UE8M0 packed, 2 UE8M0 as fp32
   int silu;       // fused silu(gate) * up
+  int masked;     // masked (EP-MoE) scheduler (else flat)
 };
 
 // Returns the __global__ function of an instance (defined in the instance TUs).

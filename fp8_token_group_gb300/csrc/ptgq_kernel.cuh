@@ -51,25 +51,36 @@ struct Slot {
   bool valid;            // the unit exists and this lane's group is inside the row
 };
 
-// Tuning parameters (compile-time): tasks per warp batch without silu (with silu: 1),
+// Tuning, per instance (compile-time), from measurements on GB300: tasks per warp batch,
 // whether the next batch's loads are issued before the current batch is computed, and the
-// CTAs per SM the register budget is sized for.
-#ifndef PTGQ_TASK_BATCH
-#define PTGQ_TASK_BATCH 2
+// CTAs per SM the register budget is sized for.  UE8M0 without silu: two tasks loaded then
+// computed, 4 CTAs/SM; fp32 scales without silu: one task, pipelined, 3 CTAs/SM; silu:
+// one task, pipelined, 2 CTAs/SM.  PTGQ_TUNE_BATCH / _PIPELINE / _MIN_BLOCKS override all
+// instances (used for sweeps).
+template <bool kPow2, bool kSilu>
+struct Tuning {
+#ifdef PTGQ_TUNE_BATCH
+  static constexpr int batch = kSilu ? 1 : PTGQ_TUNE_BATCH;
+  static constexpr bool pipeline = PTGQ_TUNE_PIPELINE;
+  static constexpr int min_blocks = PTGQ_TUNE_MIN_BLOCKS;
+#else
+  static constexpr int batch = kSilu ? 1 : (kPow2 ? 2 : 1);
+  static constexpr bool pipeline = kSilu ? true : !kPow2;
+  static constexpr int min_blocks = kSilu ? 2 : (kPow2 ? 4 : 3);
 #endif
-#ifndef PTGQ_PIPELINE
-#define PTGQ_PIPELINE 1
-#endif
-#ifndef PTGQ_MIN_BLOCKS
-#define PTGQ_MIN_BLOCKS 3
-#endif
-template <bool kSilu> struct Batch { static constexpr int n = kSilu ? 1 : PTGQ_TASK_BATCH; };
+};
 
-template <bool kFp16, bool kInt8, bool kPow2, bool kSilu>
-__global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const Params p) {
+// kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32 (the scale format
+// is a template parameter so that only the packed instances carry the exponent OR).
+template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked>
+__global__ void __launch_bounds__(kThreads, (Tuning<kFmt != 0, kSilu>::min_blocks))
+    quant_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
+  constexpr bool kPow2 = kFmt != 0;
+  constexpr bool packed = kFmt == 1;
   using Tab = SmemTables<kFp16, kSilu>;
-  constexpr int kB = Batch<kSilu>::n;
+  using Tune = Tuning<kPow2, kSilu>;
+  constexpr int kB = Tune::batch;
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Tab::bytes);
 
   // Module constants first (asynchronously): they do not depend on the previous grid.
@@ -85,8 +96,8 @@ __global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const 
   griddep_wait();
   griddep_launch_dependents();
 
-  const bool masked = p.masked_m != nullptr;
-  if (masked) masked_prefix(p.masked_m, p.n, p.rows, prefix);
+  constexpr bool masked = kMasked;
+  if constexpr (kMasked) masked_prefix(p.masked_m, p.n, p.rows, prefix);
   if constexpr (kSilu) copy_to_smem_wait();
   __syncthreads();
   const uint32_t total_units = masked ? static_cast<uint32_t>(prefix[p.n]) * p.upr : p.units_flat;
@@ -100,8 +111,6 @@ __global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const 
   const uint32_t lane_unit = lane >> lu_log2;                // unit within the warp task
   const uint32_t gj = local >> p.lg_log2;                    // group within the unit
   const uint32_t kk = local & (lg - 1u);                     // lane within the group
-  const uint32_t gmask = ((1u << lg) - 1u) << (lane & ~(lg - 1u));
-  const uint32_t umask = (lu == 32u ? 0xFFFFFFFFu : ((1u << lu) - 1u)) << (lane & ~(lu - 1u));
   const uint32_t G = 16u << p.lg_log2;
   const uint32_t total_tasks = (total_units + (1u << upw_log2) - 1u) >> upw_log2;
   const uint32_t stride = gridDim.x * kWarps;
@@ -109,7 +118,6 @@ __global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const 
   uint8_t* __restrict__ q = static_cast<uint8_t*>(p.q);
   const float* silu_tab = reinterpret_cast<const float*>(smem);
   const float rfmax = p.fmax == 448.0f ? (1.0f / 448.0f) : (1.0f / 127.0f);
-  const bool packed = p.scale_fmt == 1;
 
   // Address the lane's 16 elements of task t and start its loads.  Lanes past the end
   // (or in the unused groups of a partial unit) read a valid address of the last unit
@@ -125,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const 
     const uint32_t ge = g < p.ng ? g : p.ng - 1u;
     int64_t grow = R, sbase = 0;
     uint32_t row = R;
-    if (masked) {
+    if constexpr (kMasked) {
       const int e = expert_of(prefix, static_cast<int>(p.n), R);
       row = R - static_cast<uint32_t>(prefix[e]);
       grow = static_cast<int64_t>(e) * p.rows + row;
@@ -174,13 +182,13 @@ __global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const 
       for (int i = 0; i < 8; ++i) v[i] = widen2<kFp16>(a.w[i]);
       (void)b;
     }
-    amax_bits = redux_max(sl.valid ? amax_bits : 0u, gmask);
+    amax_bits = group_max(sl.valid ? amax_bits : 0u, lg);
     const float amax = fmaxf(u2f(amax_bits), p.eps);
     float s = div_by_const(amax, p.fmax, rfmax);
     uint32_t e = 0u;
     uint64_t y[8];
     if constexpr (kPow2) {
-      if (p.scale_floor) s = fmaxf(s, 1e-10f);
+      s = fmaxf(s, p.scale_floor);
       e = ue8m0_exponent(s);
       const float inv = ue8m0_inverse(e);
       const uint64_t inv2 = pk2(inv, inv);
@@ -208,18 +216,24 @@ __global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const 
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[i] = e4m3x2_pair(y[2 * i]) | (e4m3x2_pair(y[2 * i + 1]) << 16);
     }
-    if (sl.valid) st_128(sl.dst, o[0], o[1], o[2], o[3]);
+    st_128_if(sl.valid, sl.dst, o[0], o[1], o[2], o[3]);
 
-    if (packed) {
-      const uint32_t word = redux_or(sl.valid && kk == 0u ? (e << (8u * gj)) : 0u, umask);
-      if (sl.unit_valid && local == 0u) static_cast<uint32_t*>(p.s)[sl.sidx] = word;
-    } else if (sl.valid && kk == 0u) {
-      static_cast<float*>(p.s)[sl.sidx] = p.scale_fmt == 0 ? s : u2f(e << 23);
+    // One predicated store per lane: the packed word (unit leader), or the float scale /
+    // power of two (group leader).
+    uint32_t sval;
+    bool sp;
+    if constexpr (packed) {
+      sval = unit_or(sl.valid ? (e << (8u * gj)) : 0u, lg);
+      sp = sl.unit_valid && local == 0u;
+    } else {
+      sval = kFmt == 0 ? f2u(s) : (e << 23);
+      sp = sl.valid && kk == 0u;
     }
+    st_32_if(sp, static_cast<uint32_t*>(p.s) + sl.sidx, sval);
   };
 
   // Software pipeline: the next batch's loads are in flight while this batch computes.
-  if (total_units > 0u && !PTGQ_PIPELINE) {
+  if (total_units > 0u && !Tune::pipeline) {
     for (uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_tasks; t += kB * stride) {
       Slot cur[kB];
       Raw16 ca[kB], cb[kB];
@@ -252,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, PTGQ_MIN_BLOCKS) quant_kernel(const 
   }
 
   // Flat scheduler: zero the padding rows of out_q and of the scales.
-  if (!masked) {
+  if constexpr (!kMasked) {
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t off = p.zero_q_begin + tid * 16; off < p.zero_q_end; off += nthr * 16)
