@@ -51,35 +51,35 @@ struct Slot {
   bool valid;            // the unit exists and this lane's group is inside the row
 };
 
-// Tuning, per instance (compile-time), from measurements on GB300: tasks per warp batch,
-// whether the next batch's loads are issued before the current batch is computed, and the
-// CTAs per SM the register budget is sized for.  UE8M0 without silu: two tasks loaded then
-// computed, 4 CTAs/SM; fp32 scales without silu: one task, pipelined, 3 CTAs/SM; silu:
-// one task, pipelined, 2 CTAs/SM.  PTGQ_TUNE_BATCH / _PIPELINE / _MIN_BLOCKS override all
-// instances (used for sweeps).
-template <bool kPow2, bool kSilu>
+// Tuning, per instance (compile-time), from sweeps on GB300: tasks per warp batch, whether
+// the next batch's loads are issued before the current batch is computed, and the CTAs per
+// SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
+// CTAs/SM (64 registers); with silu: one task, pipelined, 3 CTAs/SM (2 for fp16, whose
+// per-element exponential needs the registers).
+// PTGQ_TUNE_BATCH / _PIPELINE / _MIN_BLOCKS override all instances (used for sweeps).
+template <bool kFp16, bool kSilu>
 struct Tuning {
 #ifdef PTGQ_TUNE_BATCH
   static constexpr int batch = kSilu ? 1 : PTGQ_TUNE_BATCH;
   static constexpr bool pipeline = PTGQ_TUNE_PIPELINE;
   static constexpr int min_blocks = PTGQ_TUNE_MIN_BLOCKS;
 #else
-  static constexpr int batch = kSilu ? 1 : (kPow2 ? 2 : 1);
-  static constexpr bool pipeline = kSilu ? true : !kPow2;
-  static constexpr int min_blocks = kSilu ? 2 : (kPow2 ? 4 : 3);
+  static constexpr int batch = kSilu ? 1 : 2;
+  static constexpr bool pipeline = kSilu;
+  static constexpr int min_blocks = !kSilu ? 4 : (kFp16 ? 2 : 3);
 #endif
 };
 
 // kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32 (the scale format
 // is a template parameter so that only the packed instances carry the exponent OR).
 template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked>
-__global__ void __launch_bounds__(kThreads, (Tuning<kFmt != 0, kSilu>::min_blocks))
+__global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu>::min_blocks))
     quant_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr bool kPow2 = kFmt != 0;
   constexpr bool packed = kFmt == 1;
   using Tab = SmemTables<kFp16, kSilu>;
-  using Tune = Tuning<kPow2, kSilu>;
+  using Tune = Tuning<kFp16, kSilu>;
   constexpr int kB = Tune::batch;
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Tab::bytes);
 
@@ -153,20 +153,48 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFmt != 0, kSilu>::min_block
     uint64_t v[8];                  // the 16 values as f32x2 pairs
     uint32_t amax_bits;
     if constexpr (kSilu) {
+      if constexpr (kFp16) {
+        const float2* ei = reinterpret_cast<const float2*>(silu_tab);
+        const float2* ef = ei + kExpIntWords / 2;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float s0 = silu_generic(widen_lo<true>(a.w[i]), ei, ef, PTGQ_EXP_INT_MIN, PTGQ_EXP_FRAC_JMIN);
+          const float s1 = silu_generic(widen_hi<true>(a.w[i]), ei, ef, PTGQ_EXP_INT_MIN, PTGQ_EXP_FRAC_JMIN);
+          v[i] = mul2(pk2(s0, s1), widen2<true>(b.w[i]));
+        }
+      } else {
+        // Table index = (|bits| - FIELD_LO*128) per 16-bit half, plus SPAN for a negative
+        // gate.  A gate outside the table range (|g| < 2^-25, including zero, or
+        // |g| >= 256) shows as a half >= SPAN; the first pass finds whether the warp has
+        // any, and only then does the warp take the full definition (silu_bf16).
+        constexpr uint32_t kBase = PTGQ_SILU_BF16_FIELD_LO << 7;
+        constexpr uint32_t kBase2 = kBase | (kBase << 16);
+        constexpr uint32_t kSpan = PTGQ_SILU_BF16_SPAN;
+        uint32_t dmax = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dmax = __vmaxu2(dmax, __vsub2(a.w[i] & 0x7FFF7FFFu, kBase2));
+        const bool oob = max(dmax & 0xFFFFu, dmax >> 16) >= kSpan;
+        if (!__any_sync(0xFFFFFFFFu, oob)) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t w = a.w[i];
+            const uint32_t d = __vsub2(w & 0x7FFF7FFFu, kBase2);
+            const float s0 = silu_tab[(d & 0xFFFFu) + ((w >> 15) & 1u) * kSpan];
+            const float s1 = silu_tab[(d >> 16) + (w >> 31) * kSpan];
+            v[i] = mul2(pk2(s0, s1), widen2<false>(b.w[i]));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float s0 = silu_bf16(a.w[i] & 0xFFFFu, silu_tab, PTGQ_SILU_BF16_FIELD_LO, kSpan);
+            const float s1 = silu_bf16(a.w[i] >> 16, silu_tab, PTGQ_SILU_BF16_FIELD_LO, kSpan);
+            v[i] = mul2(pk2(s0, s1), widen2<false>(b.w[i]));
+          }
+        }
+      }
       amax_bits = 0u;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        float s0, s1;
-        if constexpr (kFp16) {
-          const float2* ei = reinterpret_cast<const float2*>(silu_tab);
-          const float2* ef = ei + kExpIntWords / 2;
-          s0 = silu_generic(widen_lo<true>(a.w[i]), ei, ef, PTGQ_EXP_INT_MIN, PTGQ_EXP_FRAC_JMIN);
-          s1 = silu_generic(widen_hi<true>(a.w[i]), ei, ef, PTGQ_EXP_INT_MIN, PTGQ_EXP_FRAC_JMIN);
-        } else {
-          s0 = silu_bf16(a.w[i] & 0xFFFFu, silu_tab, PTGQ_SILU_BF16_FIELD_LO, PTGQ_SILU_BF16_SPAN);
-          s1 = silu_bf16(a.w[i] >> 16, silu_tab, PTGQ_SILU_BF16_FIELD_LO, PTGQ_SILU_BF16_SPAN);
-        }
-        v[i] = mul2(pk2(s0, s1), widen2<kFp16>(b.w[i]));
         float y0, y1;
         upk2(v[i], y0, y1);
         amax_bits = max(amax_bits, max(f2u(y0) & 0x7FFFFFFFu, f2u(y1) & 0x7FFFFFFFu));

@@ -37,13 +37,116 @@ struct PerTokenParams {
   int64_t hidden;
 };
 
-// kIn: 0 bf16, 1 fp16, 2 fp32.  kVecBytes: bytes per lane per load (16, or 8 for 16-bit
-// rows whose length is only a multiple of 4).  Each warp owns one row at a time; the
-// first kCache vectors of each lane stay in registers between the max pass and the
-// quantize pass, the rest are read again (from L2).
+template <int kIn>
+__device__ __forceinline__ uint32_t absmax_words(const uint32_t* w, int n) {
+  uint32_t m = 0u;
+  for (int k = 0; k < n; ++k) {
+    if constexpr (kIn == 2) {
+      m = max(m, w[k] & 0x7FFFFFFFu);
+    } else {
+      const uint32_t h = w[k] & 0x7FFF7FFFu;
+      m = max(m, max(h & 0xFFFFu, h >> 16));
+    }
+  }
+  return m;
+}
+
+// |x| of the 16-bit element whose magnitude pattern is m (sign cleared), as binary32 bits.
+template <int kIn>
+__device__ __forceinline__ uint32_t abs_bits(uint32_t m) {
+  if constexpr (kIn == 2) return m;
+  else return f2u(kIn == 1 ? widen_lo<true>(m) : widen_lo<false>(m));
+}
+
+// 16 bytes of input (8 16-bit or 4 binary32 elements) -> codes, stored at dst.
+template <int kIn>
+__device__ __forceinline__ void quantize16(const uint32_t (&w)[4], float inv, uint8_t* dst) {
+  if constexpr (kIn == 2) {
+    const uint32_t o = e4m3x4(__fmul_rn(u2f(w[0]), inv), __fmul_rn(u2f(w[1]), inv),
+                              __fmul_rn(u2f(w[2]), inv), __fmul_rn(u2f(w[3]), inv));
+    asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(o) : "memory");
+  } else {
+    constexpr bool h = kIn == 1;
+    const uint32_t o0 = e4m3x4(__fmul_rn(widen_lo<h>(w[0]), inv), __fmul_rn(widen_hi<h>(w[0]), inv),
+                               __fmul_rn(widen_lo<h>(w[1]), inv), __fmul_rn(widen_hi<h>(w[1]), inv));
+    const uint32_t o1 = e4m3x4(__fmul_rn(widen_lo<h>(w[2]), inv), __fmul_rn(widen_hi<h>(w[2]), inv),
+                               __fmul_rn(widen_lo<h>(w[3]), inv), __fmul_rn(widen_hi<h>(w[3]), inv));
+    asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(o0), "r"(o1) : "memory");
+  }
+}
+
+// Rows staged in shared memory.  A warp owns one row at a time and two row buffers; the
+// next row's copy (cp.async, 16 bytes per lane per instruction) is in flight while the
+// warp reduces and quantizes the current row, so each row is read from HBM once.  A lane
+// copies and later reads only its own 16-byte chunks, so the only cross-lane step is the
+// max reduction.  Rows must be a multiple of 16 bytes; the launcher sizes the CTA (32 to
+// 256 threads) so that two buffers per warp fit in shared memory.
+template <int kIn>
+__global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerTokenParams p) {
+  extern __shared__ __align__(16) unsigned char rowbuf[];
+  constexpr int kEsize = kIn == 2 ? 4 : 2;
+  constexpr int kPer16 = 16 / kEsize;                       // elements per 16-byte chunk
+  griddep_wait();
+  griddep_launch_dependents();
+  const int warps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t chunks = p.hidden / kPer16;
+  const int64_t row_bytes = chunks * 16;
+  const uint32_t buf0 = static_cast<uint32_t>(__cvta_generic_to_shared(rowbuf)) +
+                        static_cast<uint32_t>(warp * 2 * row_bytes);
+  const int64_t W = static_cast<int64_t>(gridDim.x) * warps;
+  const char* xb = static_cast<const char*>(p.x);
+
+  auto issue = [&](int64_t row, int slot) {
+    if (row < p.tokens) {
+      const char* src = xb + row * row_bytes;
+      const uint32_t dst = buf0 + static_cast<uint32_t>(slot * row_bytes);
+      for (int64_t c = lane; c < chunks; c += 32)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * static_cast<uint32_t>(c)),
+                     "l"(src + 16 * c) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  auto chunk = [&](int slot, int64_t c, uint32_t (&w)[4]) {
+    const uint32_t a = buf0 + static_cast<uint32_t>(slot * row_bytes + 16 * c);
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(a) : "memory");
+  };
+
+  int64_t row = static_cast<int64_t>(blockIdx.x) * warps + warp;
+  issue(row, 0);
+  issue(row + W, 1);
+  for (int slot = 0; row < p.tokens; row += W, slot ^= 1) {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");    // this row's copies are done
+    uint32_t m = 0u;
+    for (int64_t c = lane; c < chunks; c += 32) {
+      uint32_t w[4];
+      chunk(slot, c, w);
+      m = max(m, absmax_words<kIn>(w, 4));
+    }
+    m = redux_max(abs_bits<kIn>(m), 0xFFFFFFFFu);
+    const float s = __fdiv_rn(u2f(m), 448.0f);
+    const float inv = s == 0.0f ? 0.0f : __frcp_rn(s);
+    uint8_t* qrow = p.q + row * p.hidden;
+    for (int64_t c = lane; c < chunks; c += 32) {
+      uint32_t w[4];
+      chunk(slot, c, w);
+      quantize16<kIn>(w, inv, qrow + c * kPer16);
+    }
+    if (lane == 0) p.s[row] = s;
+    issue(row + 2 * W, slot);                              // refill this buffer
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Rows in registers (for rows the staged kernel does not take: lengths that are not a
+// multiple of 16 bytes, or too long for two shared buffers per warp).  One warp per row;
+// the first kCache vectors of each lane stay in registers between the max pass and the
+// quantize pass, the rest are read again (from L2).  kVecBytes: 16, or 8 for 16-bit rows
+// whose length is only a multiple of 4.
 template <int kIn, int kVecBytes>
-__global__ void __launch_bounds__(kThreads) per_token_kernel(const PerTokenParams p) {
-  constexpr int kElems = kIn == 2 ? kVecBytes / 4 : kVecBytes / 2;   // elements per vector
+__global__ void __launch_bounds__(kThreads) per_token_reg_kernel(const PerTokenParams p) {
+  constexpr int kElems = kIn == 2 ? kVecBytes / 4 : kVecBytes / 2;
   constexpr int kWords = kVecBytes / 4;
   constexpr int kCache = 8;
   griddep_wait();
@@ -62,41 +165,15 @@ __global__ void __launch_bounds__(kThreads) per_token_kernel(const PerTokenParam
       asm volatile("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(ptr));
     }
   };
-  auto absmax = [&](const uint32_t (&w)[kWords]) {
-    uint32_t m = 0u;
-#pragma unroll
-    for (int k = 0; k < kWords; ++k) {
-      if constexpr (kIn == 2) {
-        m = max(m, w[k] & 0x7FFFFFFFu);
-      } else {
-        const uint32_t h = w[k] & 0x7FFF7FFFu;
-        const uint32_t hm = max(h & 0xFFFFu, h >> 16);
-        m = max(m, f2u(kIn == 1 ? widen_lo<true>(hm) : widen_lo<false>(hm)));
-      }
-    }
-    return m;
-  };
   auto quantize_store = [&](int64_t row, int64_t i, const uint32_t (&w)[kWords], float inv) {
-    float v[kElems];
-#pragma unroll
-    for (int k = 0; k < kWords; ++k) {
-      if constexpr (kIn == 2) {
-        v[k] = u2f(w[k]);
-      } else {
-        v[2 * k] = kIn == 1 ? widen_lo<true>(w[k]) : widen_lo<false>(w[k]);
-        v[2 * k + 1] = kIn == 1 ? widen_hi<true>(w[k]) : widen_hi<false>(w[k]);
-      }
-    }
-    uint32_t o[kElems / 4];
-#pragma unroll
-    for (int k = 0; k < kElems / 4; ++k)
-      o[k] = e4m3x4(__fmul_rn(v[4 * k], inv), __fmul_rn(v[4 * k + 1], inv),
-                    __fmul_rn(v[4 * k + 2], inv), __fmul_rn(v[4 * k + 3], inv));
     uint8_t* dst = p.q + row * p.hidden + i * kElems;
-    if constexpr (kElems == 8) {
-      asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(o[0]), "r"(o[1]) : "memory");
-    } else {
-      asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(o[0]) : "memory");
+    if constexpr (kVecBytes == 16) {
+      quantize16<kIn>(w, inv, dst);
+    } else {       // 16-bit, 4 elements
+      constexpr bool h = kIn == 1;
+      const uint32_t o = e4m3x4(__fmul_rn(widen_lo<h>(w[0]), inv), __fmul_rn(widen_hi<h>(w[0]), inv),
+                                __fmul_rn(widen_lo<h>(w[1]), inv), __fmul_rn(widen_hi<h>(w[1]), inv));
+      asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(o) : "memory");
     }
   };
 
@@ -109,15 +186,15 @@ __global__ void __launch_bounds__(kThreads) per_token_kernel(const PerTokenParam
       const int64_t i = lane + 32 * j;
       if (i < nvec) {
         load(row, i, cache[j]);
-        m = max(m, absmax(cache[j]));
+        m = max(m, absmax_words<kIn>(cache[j], kWords));
       }
     }
     for (int64_t i = lane + 32 * kCache; i < nvec; i += 32) {
       uint32_t w[kWords];
       load(row, i, w);
-      m = max(m, absmax(w));
+      m = max(m, absmax_words<kIn>(w, kWords));
     }
-    m = redux_max(m, 0xFFFFFFFFu);
+    m = redux_max(abs_bits<kIn>(m), 0xFFFFFFFFu);
     const float s = __fdiv_rn(u2f(m), 448.0f);
     const float inv = s == 0.0f ? 0.0f : __frcp_rn(s);
 #pragma unroll
@@ -213,7 +290,7 @@ std::mutex g_mu;
 std::map<std::tuple<const void*, int, size_t>, int> g_occ;   // (kernel, device, smem) -> blocks/SM
 std::map<int, int> g_sms;
 
-int grid_for(const void* fn, size_t smem, int64_t want) {
+int grid_for(const void* fn, size_t smem, int64_t want, int threads = kThreads) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -223,21 +300,26 @@ int grid_for(const void* fn, size_t smem, int64_t want) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
     s = g_sms.emplace(dev, n).first;
   }
-  auto o = g_occ.find(std::make_tuple(fn, dev, smem));
+  auto o = g_occ.find(std::make_tuple(fn, dev, smem + static_cast<size_t>(threads) * 1000000u));
   if (o == g_occ.end()) {
-    int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kThreads, smem) != cudaSuccess || nb < 1)
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
       return -1;
-    o = g_occ.emplace(std::make_tuple(fn, dev, smem), nb).first;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess || nb < 1)
+      return -1;
+    o = g_occ.emplace(std::make_tuple(fn, dev, smem + static_cast<size_t>(threads) * 1000000u), nb).first;
   }
   const int64_t full = static_cast<int64_t>(o->second) * s->second;
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, full)));
 }
 
-int launch(const void* fn, int grid, size_t smem, ptgq_stream_t stream, void** args) {
+int launch(const void* fn, int grid, size_t smem, ptgq_stream_t stream, void** args,
+           int threads = kThreads) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
@@ -250,13 +332,21 @@ int launch(const void* fn, int grid, size_t smem, ptgq_stream_t stream, void** a
   return PTGQ_OK;
 }
 
-const void* per_token_fn(int dtype, bool wide) {
+const void* per_token_reg_fn(int dtype, bool wide) {
   switch (dtype * 2 + (wide ? 1 : 0)) {
-    case 0: return reinterpret_cast<const void*>(&per_token_kernel<0, 8>);
-    case 1: return reinterpret_cast<const void*>(&per_token_kernel<0, 16>);
-    case 2: return reinterpret_cast<const void*>(&per_token_kernel<1, 8>);
-    case 3: return reinterpret_cast<const void*>(&per_token_kernel<1, 16>);
-    default: return reinterpret_cast<const void*>(&per_token_kernel<2, 16>);
+    case 0: return reinterpret_cast<const void*>(&per_token_reg_kernel<0, 8>);
+    case 1: return reinterpret_cast<const void*>(&per_token_reg_kernel<0, 16>);
+    case 2: return reinterpret_cast<const void*>(&per_token_reg_kernel<1, 8>);
+    case 3: return reinterpret_cast<const void*>(&per_token_reg_kernel<1, 16>);
+    default: return reinterpret_cast<const void*>(&per_token_reg_kernel<2, 16>);
+  }
+}
+
+const void* per_token_smem_fn(int dtype) {
+  switch (dtype) {
+    case 0: return reinterpret_cast<const void*>(&per_token_smem_kernel<0>);
+    case 1: return reinterpret_cast<const void*>(&per_token_smem_kernel<1>);
+    default: return reinterpret_cast<const void*>(&per_token_smem_kernel<2>);
   }
 }
 
@@ -281,11 +371,25 @@ extern "C" int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens
   if (reinterpret_cast<uintptr_t>(x) % need != 0 || reinterpret_cast<uintptr_t>(out_q) % (wide && esize == 2 ? 8 : 4) != 0 ||
       reinterpret_cast<uintptr_t>(out_s) % 4 != 0)
     return PTGQ_ERR_ALIGN;
-  const void* fn = per_token_fn(dtype, wide);
-  const int grid = grid_for(fn, 0, (num_tokens + kWarps - 1) / kWarps);
-  if (grid < 0) return PTGQ_ERR_CUDA;
   PerTokenParams p{x, static_cast<uint8_t*>(out_q), out_s, num_tokens, hidden};
   void* args[] = {&p};
+  // Staged kernel: rows that are a multiple of 16 bytes and of which two fit per warp in
+  // a 200 KB shared-memory budget with at least two warps per CTA.
+  const int64_t row_bytes = hidden * esize;
+  constexpr int64_t kSmemBudget = 200 * 1024;
+  const int64_t warps_fit = kSmemBudget / (2 * row_bytes);
+  if (row_bytes % 16 == 0 && row_bytes >= 512 && warps_fit >= 2 &&
+      reinterpret_cast<uintptr_t>(x) % 16 == 0) {
+    const int warps = static_cast<int>(std::min<int64_t>(kWarps, warps_fit));
+    const size_t smem = static_cast<size_t>(warps) * 2 * static_cast<size_t>(row_bytes);
+    const void* fn = per_token_smem_fn(dtype);
+    const int grid = grid_for(fn, smem, (num_tokens + warps - 1) / warps, 32 * warps);
+    if (grid < 0) return PTGQ_ERR_CUDA;
+    return launch(fn, grid, smem, stream, args, 32 * warps);
+  }
+  const void* fn = per_token_reg_fn(dtype, wide);
+  const int grid = grid_for(fn, 0, (num_tokens + kWarps - 1) / kWarps);
+  if (grid < 0) return PTGQ_ERR_CUDA;
   return launch(fn, grid, 0, stream, args);
 }
 
