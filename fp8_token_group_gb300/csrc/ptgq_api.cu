@@ -132,16 +132,20 @@ int launch_blocks(const void* fn, int dev, size_t smem, int* blocks_per_sm, int*
   auto at = g_smem_attr.find(akey);
   if (smem > 48 * 1024 && (at == g_smem_attr.end() || at->second < smem)) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+                             static_cast<int>(smem)) != cudaSuccess) {
+      cudaGetLastError();
       return PTGQ_ERR_CUDA;
+    }
     g_smem_attr[akey] = smem;
   }
   const auto okey = std::make_tuple(fn, dev, smem);
   auto ot = g_occupancy.find(okey);
   if (ot == g_occupancy.end()) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kThreads, smem) != cudaSuccess || nb < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kThreads, smem) != cudaSuccess || nb < 1) {
+      cudaGetLastError();
       return PTGQ_ERR_CUDA;
+    }
     ot = g_occupancy.emplace(okey, nb).first;
   }
   *blocks_per_sm = ot->second;
@@ -227,7 +231,12 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   cfg.attrs = attr;
   cfg.numAttrs = (flags & PTGQ_FLAG_NO_PDL) ? 0 : 1;
   void* args[] = {&p};
-  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return PTGQ_ERR_CUDA;
+  // A failed launch is reported through the status code; the runtime's error state is
+  // cleared so it does not surface later in the caller's own CUDA calls.
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return PTGQ_ERR_CUDA;
+  }
   if (cudaGetLastError() != cudaSuccess) return PTGQ_ERR_CUDA;
   return PTGQ_OK;
 }

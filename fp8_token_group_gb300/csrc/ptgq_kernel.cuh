@@ -54,10 +54,10 @@ struct Slot {
 // Tuning, per instance (compile-time), from sweeps on GB300: tasks per warp batch, whether
 // the next batch's loads are issued before the current batch is computed, and the CTAs per
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
-// CTAs/SM (64 registers); with silu: one task, pipelined, 3 CTAs/SM (2 for fp16, whose
-// per-element exponential needs the registers).
-// PTGQ_TUNE_BATCH / _PIPELINE / _MIN_BLOCKS override all instances (used for sweeps).
-template <bool kFp16, bool kSilu>
+// CTAs/SM (64 registers).  bf16 silu: flat pipelined at 3 CTAs/SM, masked unpipelined at
+// 4 CTAs/SM.  fp16 silu: pipelined at 2 CTAs/SM (its per-element exponential needs the
+// registers).  PTGQ_TUNE_BATCH / _PIPELINE / _MIN_BLOCKS override all instances (sweeps).
+template <bool kFp16, bool kSilu, bool kMasked>
 struct Tuning {
 #ifdef PTGQ_TUNE_BATCH
   static constexpr int batch = kSilu ? 1 : PTGQ_TUNE_BATCH;
@@ -65,21 +65,21 @@ struct Tuning {
   static constexpr int min_blocks = PTGQ_TUNE_MIN_BLOCKS;
 #else
   static constexpr int batch = kSilu ? 1 : 2;
-  static constexpr bool pipeline = kSilu;
-  static constexpr int min_blocks = !kSilu ? 4 : (kFp16 ? 2 : 3);
+  static constexpr bool pipeline = kSilu && (kFp16 || !kMasked);
+  static constexpr int min_blocks = !kSilu ? 4 : (kFp16 ? 2 : (kMasked ? 4 : 3));
 #endif
 };
 
 // kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32 (the scale format
 // is a template parameter so that only the packed instances carry the exponent OR).
 template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked>
-__global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu>::min_blocks))
+__global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_blocks))
     quant_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr bool kPow2 = kFmt != 0;
   constexpr bool packed = kFmt == 1;
   using Tab = SmemTables<kFp16, kSilu>;
-  using Tune = Tuning<kFp16, kSilu>;
+  using Tune = Tuning<kFp16, kSilu, kMasked>;
   constexpr int kB = Tune::batch;
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Tab::bytes);
 

@@ -289,10 +289,14 @@ namespace {
 std::mutex g_mu;
 std::map<std::tuple<const void*, int, size_t>, int> g_occ;   // (kernel, device, smem) -> blocks/SM
 std::map<int, int> g_sms;
+std::map<std::pair<const void*, int>, size_t> g_smem_attr;   // (kernel, device) -> attribute set
 
 int grid_for(const void* fn, size_t smem, int64_t want, int threads = kThreads) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   auto s = g_sms.find(dev);
   if (s == g_sms.end()) {
@@ -300,15 +304,26 @@ int grid_for(const void* fn, size_t smem, int64_t want, int threads = kThreads) 
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
     s = g_sms.emplace(dev, n).first;
   }
+  // The dynamic shared-memory limit of a kernel is only ever raised, so a launch with a
+  // size seen earlier stays valid after launches with smaller sizes.
+  if (smem > 48 * 1024) {
+    auto a = g_smem_attr.find({fn, dev});
+    if (a == g_smem_attr.end() || a->second < smem) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+      }
+      g_smem_attr[{fn, dev}] = smem;
+    }
+  }
   auto o = g_occ.find(std::make_tuple(fn, dev, smem + static_cast<size_t>(threads) * 1000000u));
   if (o == g_occ.end()) {
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess)
-      return -1;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess || nb < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess || nb < 1) {
+      cudaGetLastError();
       return -1;
+    }
     o = g_occ.emplace(std::make_tuple(fn, dev, smem + static_cast<size_t>(threads) * 1000000u), nb).first;
   }
   const int64_t full = static_cast<int64_t>(o->second) * s->second;
@@ -327,7 +342,12 @@ int launch(const void* fn, int grid, size_t smem, ptgq_stream_t stream, void** a
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return PTGQ_ERR_CUDA;
+  // A failed launch is reported through the status code; the runtime's error state is
+  // cleared so it does not surface later in the caller's own CUDA calls.
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    cudaGetLastError();
+    return PTGQ_ERR_CUDA;
+  }
   if (cudaGetLastError() != cudaSuccess) return PTGQ_ERR_CUDA;
   return PTGQ_OK;
 }

@@ -106,3 +106,12 @@ def test_requant_random_codes_scales_and_saturation(group):
     assert np.array_equal(got, ref)
     got, ref = _requant_both(codes, xs, (M * (K // group), K // group, 1), None, 0.61, group)
     assert np.array_equal(got, ref)
+
+
+def test_per_token_row_sizes_in_any_order():
+    """The staged kernel's shared-memory size depends on the row length; calls with a long
+    row, then a short one, then the long one again must all launch."""
+    for hidden in (4096, 512, 4096, 1024, 3072):
+        x = synth.sweep_input(hidden, 64, hidden, torch.float32)
+        gq, gs, oq, os_ = _per_token_both(x, 64)
+        assert np.array_equal(gq, oq) and np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
