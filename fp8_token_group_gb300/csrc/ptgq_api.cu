@@ -34,7 +34,8 @@ const void* kernel_for(const KernelKey& k) {
 
 size_t dynamic_smem_bytes(const KernelKey& k, int64_t experts) {
   const size_t tab = static_cast<size_t>(k.fp16 ? table_bytes_fp16(k.silu) : table_bytes_bf16(k.silu));
-  return tab + (experts > 0 ? static_cast<size_t>(experts + 1) * sizeof(int32_t) : 0);
+  // masked: prefix of the live-row counts (E + 1) and the row-to-expert buckets
+  return tab + (experts > 0 ? static_cast<size_t>(experts + 1 + kBuckets + 1) * sizeof(int32_t) : 0);
 }
 
 namespace {

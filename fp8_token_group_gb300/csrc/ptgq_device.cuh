@@ -125,6 +125,34 @@ __device__ __forceinline__ void masked_prefix(const int32_t* __restrict__ masked
   if (tid == kThreads - 1) prefix[n] = base + incl;
 }
 
+// Rows-to-expert buckets for the masked scheduler: bucket[b] is the expert of live row
+// min(b << shift, live - 1) for b = 0..kBuckets, with shift the smallest value that maps
+// every live row to a bucket below kBuckets.  A lookup then searches only between two
+// neighbouring buckets' experts (usually zero or one step) instead of over all experts.
+__device__ __forceinline__ int expert_in(const int32_t* prefix, int lo, int hi, uint32_t R) {
+  // largest e in [lo, hi] with prefix[e] <= R
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<uint32_t>(prefix[mid]) <= R) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ uint32_t bucket_shift(uint32_t live) {
+  const uint32_t top = live > 0u ? live - 1u : 0u;
+  const int bits = 32 - __clz(top);                 // bits needed for the largest row
+  return bits > 8 ? static_cast<uint32_t>(bits - 8) : 0u;
+}
+
+__device__ __forceinline__ void build_buckets(const int32_t* prefix, int n, uint32_t live,
+                                              uint32_t shift, int32_t* bucket) {
+  for (int b = threadIdx.x; b <= kBuckets; b += kThreads) {
+    const uint32_t r0 = min(static_cast<uint32_t>(b) << shift, live > 0u ? live - 1u : 0u);
+    bucket[b] = expert_in(prefix, 0, n - 1, r0);
+  }
+}
+
 // Largest e in [0, n) with prefix[e] <= R (an expert that owns live row R).
 __device__ __forceinline__ int expert_of(const int32_t* prefix, int n, uint32_t R) {
   int lo = 0, hi = n;

@@ -10,6 +10,7 @@ namespace ptgq {
 constexpr int kThreads = 256;                 // 8 warps per CTA
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxExperts = 4096;             // masked scheduler: E <= kMaxExperts
+constexpr int kBuckets = 256;                 // masked scheduler: row-to-expert buckets
 
 // Work decomposition.  A "unit" is one group (float scale formats) or four
 // consecutive groups of one row (packed UE8M0, so one unit fills one int32 word).

@@ -97,7 +97,14 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
   griddep_launch_dependents();
 
   constexpr bool masked = kMasked;
-  if constexpr (kMasked) masked_prefix(p.masked_m, p.n, p.rows, prefix);
+  int32_t* bucket = prefix + (p.n + 1);
+  uint32_t bshift = 0u;
+  if constexpr (kMasked) {
+    masked_prefix(p.masked_m, p.n, p.rows, prefix);
+    __syncthreads();
+    bshift = bucket_shift(static_cast<uint32_t>(prefix[p.n]));
+    build_buckets(prefix, static_cast<int>(p.n), static_cast<uint32_t>(prefix[p.n]), bshift, bucket);
+  }
   if constexpr (kSilu) copy_to_smem_wait();
   __syncthreads();
   const uint32_t total_units = masked ? static_cast<uint32_t>(prefix[p.n]) * p.upr : p.units_flat;
@@ -134,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
     int64_t grow = R, sbase = 0;
     uint32_t row = R;
     if constexpr (kMasked) {
-      const int e = expert_of(prefix, static_cast<int>(p.n), R);
+      const uint32_t b = R >> bshift;
+      const int e = expert_in(prefix, bucket[b], bucket[b + 1], R);
       row = R - static_cast<uint32_t>(prefix[e]);
       grow = static_cast<int64_t>(e) * p.rows + row;
       sbase = static_cast<int64_t>(e) * p.s_per_block;

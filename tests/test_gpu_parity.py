@@ -316,3 +316,18 @@ def test_device_arguments_rejected_before_launch():
     rc = L.ptgq_quant(x.data_ptr(), 0, 4, 2, 256, 128, q.data_ptr(), 0, s.data_ptr(), 0, 0, 0,
                       None, 1e-10, stream)
     assert rc == -6
+
+
+def test_masked_4096_experts_mostly_empty():
+    """The largest expert count, with many empty and one-row experts: exercises the
+    row-to-expert buckets across runs of empty experts."""
+    E, tp = 4096, 3
+    x = synth.normal((E, tp, 256), torch.bfloat16, seed=4)
+    g = torch.Generator().manual_seed(11)
+    mm = torch.randint(0, 4, (E,), generator=g, dtype=torch.int32)
+    mm[torch.rand(E, generator=g) < 0.7] = 0          # 70% of experts empty
+    mm[-1] = 3
+    for fmt in FMTS:
+        compare(x, Case(scale_fmt=fmt, layout=P.COL_MAJOR_TMA), masked_m=mm.numpy())
+    compare(torch.cat([x, x], 2), Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED,
+                                       layout=P.COL_MAJOR_TMA), masked_m=mm.numpy())
