@@ -135,18 +135,22 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
           scale_fmt: int = SCALE_FP32, scale_layout: int = ROW_MAJOR, fuse_silu: bool = False,
           masked_m=None, eps: float = 1e-10, tokens_pad: int = 0, flags: int = 0,
           stream=None) -> None:
-    """Quantize ``x`` into the caller's ``out_q`` / ``out_s`` (device tensors) on ``stream``
-    (default: torch's current stream).  Arguments follow ``ptgq_quant`` in include/ptgq.h."""
+    """Quantize ``x`` into the caller's ``out_q`` / ``out_s`` on ``stream`` (default: torch's
+    current stream).  Tensors must be device-accessible: CUDA tensors, or pinned host tensors,
+    which the GPU reads and writes in place over the host link (unified addressing).
+    Arguments follow ``ptgq_quant`` in include/ptgq.h."""
     import torch
-    if not x.is_cuda:
-        raise ValueError("x must be a CUDA tensor (use quantize() for host tensors)")
+    for name, t in (("x", x), ("out_q", out_q), ("out_s", out_s)):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory "
+                             "(use quantize() for pageable host tensors)")
     if not (x.is_contiguous() and out_q.is_contiguous() and out_s.is_contiguous()):
         raise ValueError("x, out_q and out_s must be contiguous")
     if out_dtype is None:
         out_dtype = INT8 if out_q.dtype == torch.int8 else E4M3
     if masked_m is not None:
-        if masked_m.dtype != torch.int32 or not masked_m.is_cuda:
-            raise ValueError("masked_m must be a CUDA int32 tensor")
+        if masked_m.dtype != torch.int32 or not (masked_m.is_cuda or masked_m.is_pinned()):
+            raise ValueError("masked_m must be a device-accessible int32 tensor")
         E, tp, hin = x.shape
         n, tokens_pad = E, tp
         if E == 0:
@@ -155,7 +159,7 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
         n, hin = x.shape
     H = hin // 2 if fuse_silu else hin
     if stream is None:
-        stream = torch.cuda.current_stream(x.device)
+        stream = torch.cuda.current_stream(x.device if x.is_cuda else None)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     rc = lib().ptgq_quant_ex(
         x.data_ptr(), _in_dtype(x), n, tokens_pad, H, group_size, out_q.data_ptr(), out_dtype,

@@ -75,12 +75,21 @@ __device__ __forceinline__ void quantize16(const uint32_t (&w)[4], float inv, ui
   }
 }
 
-// Rows staged in shared memory.  A warp owns one row at a time and two row buffers; the
-// next row's copy (cp.async, 16 bytes per lane per instruction) is in flight while the
-// warp reduces and quantizes the current row, so each row is read from HBM once.  A lane
-// copies and later reads only its own 16-byte chunks, so the only cross-lane step is the
-// max reduction.  Rows must be a multiple of 16 bytes; the launcher sizes the CTA (32 to
-// 256 threads) so that two buffers per warp fit in shared memory.
+// Rows staged in shared memory.  A warp owns one row at a time and kBufs row buffers; the
+// copies of its next kBufs-1 rows (cp.async, 16 bytes per lane per instruction) are in
+// flight while the warp reduces and quantizes the current row, so each row is read from
+// HBM once.  A lane copies and later reads only its own 16-byte chunks, so the only
+// cross-lane step is the max reduction.  Rows must be a multiple of 16 bytes; the launcher
+// sizes the CTA (32 to 256 threads) so that kBufs buffers per warp fit in shared memory.
+#ifndef PTGQ_PT_BUFS
+#define PTGQ_PT_BUFS 2
+#endif
+#ifndef PTGQ_PT_WARPS
+#define PTGQ_PT_WARPS 8
+#endif
+constexpr int kPtBufs = PTGQ_PT_BUFS;        // row buffers per warp
+constexpr int kPtWarps = PTGQ_PT_WARPS;      // most warps per CTA
+
 template <int kIn>
 __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerTokenParams p) {
   extern __shared__ __align__(16) unsigned char rowbuf[];
@@ -93,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerToken
   const int64_t chunks = p.hidden / kPer16;
   const int64_t row_bytes = chunks * 16;
   const uint32_t buf0 = static_cast<uint32_t>(__cvta_generic_to_shared(rowbuf)) +
-                        static_cast<uint32_t>(warp * 2 * row_bytes);
+                        static_cast<uint32_t>(warp * kPtBufs * row_bytes);
   const int64_t W = static_cast<int64_t>(gridDim.x) * warps;
   const char* xb = static_cast<const char*>(p.x);
 
@@ -114,10 +123,11 @@ __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerToken
   };
 
   int64_t row = static_cast<int64_t>(blockIdx.x) * warps + warp;
-  issue(row, 0);
-  issue(row + W, 1);
-  for (int slot = 0; row < p.tokens; row += W, slot ^= 1) {
-    asm volatile("cp.async.wait_group 1;" ::: "memory");    // this row's copies are done
+#pragma unroll
+  for (int b = 0; b < kPtBufs; ++b) issue(row + b * W, b);
+  for (int slot = 0; row < p.tokens; row += W, slot = slot + 1 == kPtBufs ? 0 : slot + 1) {
+    // all but the kPtBufs-1 most recent groups are complete: this row's copies are done
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPtBufs - 1) : "memory");
     uint32_t m = 0u;
     for (int64_t c = lane; c < chunks; c += 32) {
       uint32_t w[4];
@@ -134,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerToken
       quantize16<kIn>(w, inv, qrow + c * kPer16);
     }
     if (lane == 0) p.s[row] = s;
-    issue(row + 2 * W, slot);                              // refill this buffer
+    issue(row + kPtBufs * W, slot);                        // refill this buffer
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -393,15 +403,15 @@ extern "C" int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens
     return PTGQ_ERR_ALIGN;
   PerTokenParams p{x, static_cast<uint8_t*>(out_q), out_s, num_tokens, hidden};
   void* args[] = {&p};
-  // Staged kernel: rows that are a multiple of 16 bytes and of which two fit per warp in
-  // a 200 KB shared-memory budget with at least two warps per CTA.
+  // Staged kernel: rows that are a multiple of 16 bytes and of which kPtBufs fit per warp
+  // in a 200 KB shared-memory budget with at least two warps per CTA.
   const int64_t row_bytes = hidden * esize;
   constexpr int64_t kSmemBudget = 200 * 1024;
-  const int64_t warps_fit = kSmemBudget / (2 * row_bytes);
+  const int64_t warps_fit = kSmemBudget / (kPtBufs * row_bytes);
   if (row_bytes % 16 == 0 && row_bytes >= 512 && warps_fit >= 2 &&
       reinterpret_cast<uintptr_t>(x) % 16 == 0) {
-    const int warps = static_cast<int>(std::min<int64_t>(kWarps, warps_fit));
-    const size_t smem = static_cast<size_t>(warps) * 2 * static_cast<size_t>(row_bytes);
+    const int warps = static_cast<int>(std::min<int64_t>(kPtWarps, warps_fit));
+    const size_t smem = static_cast<size_t>(warps) * kPtBufs * static_cast<size_t>(row_bytes);
     const void* fn = per_token_smem_fn(dtype);
     const int grid = grid_for(fn, smem, (num_tokens + warps - 1) / warps, 32 * warps);
     if (grid < 0) return PTGQ_ERR_CUDA;

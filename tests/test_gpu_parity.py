@@ -331,3 +331,19 @@ def test_masked_4096_experts_mostly_empty():
         compare(x, Case(scale_fmt=fmt, layout=P.COL_MAJOR_TMA), masked_m=mm.numpy())
     compare(torch.cat([x, x], 2), Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED,
                                        layout=P.COL_MAJOR_TMA), masked_m=mm.numpy())
+
+
+def test_pinned_host_buffers_in_place():
+    """Pinned host tensors are device-accessible (unified addressing): quantizing them in
+    place gives the same bytes as device buffers."""
+    x = synth.flat_outliers(256, 7168)
+    c = Case(scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA)
+    gq, gs = run_gpu(x, c)
+    xh = x.pin_memory()
+    qh = torch.empty((256, 7168), dtype=torch.float8_e4m3fn).pin_memory()
+    sh = torch.empty(P.scale_elems(256, 0, 7168, 128, c.scale_fmt, c.layout, False),
+                     dtype=torch.int32).pin_memory()
+    P.quant(xh, qh, sh, 128, scale_fmt=c.scale_fmt, scale_layout=c.layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(qh.view(torch.uint8).numpy().ravel(), gq)
+    assert np.array_equal(sh.numpy().view(np.uint32), gs)
