@@ -13,8 +13,8 @@
 //            sum in shared memory, so work is dealt out over live rows only and no
 //            CTA is spent on dead rows.
 // Per lane: one 256-bit load of 16 contiguous 16-bit elements (two with silu:
-// gate and up), amax in registers, group amax with redux.sync over the G/16
-// lanes of the group, scale and codes in binary32, one 128-bit store of 16
+// gate and up), amax in registers, group amax with a butterfly of shuffles over
+// the G/16 lanes of the group, scale and codes in binary32, one 128-bit store of 16
 // codes.  Packed UE8M0 exponents of four groups are OR-reduced into one int32
 // word and stored by one lane.  Launched with programmatic dependent launch: the
 // kernel waits on griddepcontrol before its first access to caller memory.

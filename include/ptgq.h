@@ -20,11 +20,12 @@
  *   that definition (the library is tested against an independent CPU oracle).
  *
  * Conventions for every entry point:
- *   - Pointers named x, out_q, out_s, masked_m are DEVICE pointers (cudaMalloc or a
- *     torch CUDA tensor) on the current device.  The caller owns every buffer; the
- *     library allocates nothing, never synchronises, never reads device memory on
- *     the host, and launches at most one kernel per call on `stream`, so a call can
- *     be captured in a CUDA graph.
+ *   - Buffer pointers (x, out_q, out_s, masked_m, ...) are addresses the current device
+ *     can access: device memory (cudaMalloc, a torch CUDA tensor), or page-locked host
+ *     memory under unified addressing, which the kernel then reads and writes in place
+ *     over the host link.  The caller owns every buffer; the library allocates nothing,
+ *     never synchronises, never dereferences a buffer on the host, and launches at most
+ *     one kernel per call on `stream`, so a call can be captured in a CUDA graph.
  *   - Errors are returned as negative status codes (below) before anything is
  *     launched; nothing is written in that case.  No exception crosses the ABI.
  *     PTGQ_ERR_CUDA reports a launch failure taken from cudaGetLastError().
