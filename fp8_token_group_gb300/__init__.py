@@ -21,7 +21,8 @@ import threading
 
 __all__ = [
     "BF16", "FP16", "FP32", "E4M3", "INT8", "SCALE_FP32", "SCALE_UE8M0_PACKED", "SCALE_UE8M0_FP32",
-    "ROW_MAJOR", "COL_MAJOR_TMA", "FLAG_NO_PDL", "FLAG_UE8M0_SCALE_FLOOR", "EPS_MIN",
+    "ROW_MAJOR", "COL_MAJOR_TMA", "FLAG_NO_PDL", "FLAG_UE8M0_SCALE_FLOOR", "FLAG_FAST_DIVIDE",
+    "EPS_MIN",
     "PtgqError", "lib", "lib_path", "header_functions", "quant", "quantize", "scale_elems",
     "alloc_outputs", "strerror", "per_token_quant", "requant_per_tensor",
 ]
@@ -30,7 +31,7 @@ BF16, FP16, FP32 = 0, 1, 2
 E4M3, INT8 = 0, 1
 SCALE_FP32, SCALE_UE8M0_PACKED, SCALE_UE8M0_FP32 = 0, 1, 2
 ROW_MAJOR, COL_MAJOR_TMA = 0, 1
-FLAG_NO_PDL, FLAG_UE8M0_SCALE_FLOOR = 1, 2
+FLAG_NO_PDL, FLAG_UE8M0_SCALE_FLOOR, FLAG_FAST_DIVIDE = 1, 2, 4
 EPS_MIN = 1e-24
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -88,7 +88,8 @@ int validate(const void* x, int dtype, int64_t n, int64_t tokens_pad, int64_t hi
     return PTGQ_ERR_GROUP;
   if (hidden <= 0 || hidden % group_size != 0) return PTGQ_ERR_HIDDEN;
   if ((fuse_silu != 0 && fuse_silu != 1) ||
-      (flags & ~static_cast<unsigned>(PTGQ_FLAG_NO_PDL | PTGQ_FLAG_UE8M0_SCALE_FLOOR)) != 0)
+      (flags & ~static_cast<unsigned>(PTGQ_FLAG_NO_PDL | PTGQ_FLAG_UE8M0_SCALE_FLOOR |
+                                   PTGQ_FLAG_FAST_DIVIDE)) != 0)
     return PTGQ_ERR_FLAG;
   const bool masked = masked_m != nullptr;
   if (n < 0 || tokens_pad < 0) return PTGQ_ERR_SHAPE;
@@ -200,7 +201,9 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
     p.zero_s_rows = (scale_layout == PTGQ_ROW_MAJOR ? g.rows : g.mn_pad) - n;
   }
 
-  const KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, scale_fmt, fuse_silu, masked};
+  // Internal format 3: fp32 scales with approximate element division (fast-math interop).
+  const int kfmt = (scale_fmt == PTGQ_SCALE_FP32 && (flags & PTGQ_FLAG_FAST_DIVIDE)) ? 3 : scale_fmt;
+  const KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, kfmt, fuse_silu, masked};
   const void* fn = kernel_for(key);
   const size_t smem = dynamic_smem_bytes(key, masked ? n : 0);
   int dev = 0;

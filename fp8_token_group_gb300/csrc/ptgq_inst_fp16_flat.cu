@@ -5,21 +5,25 @@
 namespace ptgq {
 
 const void* kernel_for_fp16_flat(int int8, int fmt, int silu) {
-  static const void* const table[12] = {
+  static const void* const table[16] = {
       reinterpret_cast<const void*>(&quant_kernel<true, false, 0, false, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, false, 0, true, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, false, 1, false, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, false, 1, true, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, false, 2, false, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, false, 2, true, false>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 3, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 3, true, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, true, 0, false, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, true, 0, true, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, true, 1, false, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, true, 1, true, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, true, 2, false, false>),
       reinterpret_cast<const void*>(&quant_kernel<true, true, 2, true, false>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 3, false, false>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 3, true, false>),
   };
-  return table[(int8 ? 6 : 0) + fmt * 2 + (silu ? 1 : 0)];
+  return table[(int8 ? 8 : 0) + fmt * 2 + (silu ? 1 : 0)];
 }
 
 int table_bytes_fp16(int silu) { return silu ? SmemTables<true, true>::bytes : 0; }

@@ -52,7 +52,7 @@ struct Params {
 struct KernelKey {
   int fp16;       // input is fp16 (else bf16)
   int int8;       // output is int8 (else e4m3)
-  int fmt;        // scale format: 0 fp32, 1 UE8M0 packed, 2 UE8M0 as fp32
+  int fmt;        // 0 fp32, 1 UE8M0 packed, 2 UE8M0 as fp32, 3 fp32 with approximate division
   int silu;       // fused silu(gate) * up
   int masked;     // masked (EP-MoE) scheduler (else flat)
 };

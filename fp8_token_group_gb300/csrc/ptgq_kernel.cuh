@@ -70,13 +70,14 @@ struct Tuning {
 #endif
 };
 
-// kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32 (the scale format
-// is a template parameter so that only the packed instances carry the exponent OR).
+// kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32, 3 fp32 scales with
+// the element quotients taken by approximate division (fast-math interop).  The scale
+// format is a template parameter so that only the packed instances carry the exponent OR.
 template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked>
 __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_blocks))
     quant_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr bool kPow2 = kFmt != 0;
+  constexpr bool kPow2 = kFmt == 1 || kFmt == 2;
   constexpr bool packed = kFmt == 1;
   using Tab = SmemTables<kFp16, kSilu>;
   using Tune = Tuning<kFp16, kSilu, kMasked>;
@@ -230,6 +231,13 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
       const uint64_t inv2 = pk2(inv, inv);
 #pragma unroll
       for (int i = 0; i < 8; ++i) y[i] = mul2(v[i], inv2);
+    } else if constexpr (kFmt == 3) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float v0, v1;
+        upk2(v[i], v0, v1);
+        y[i] = pk2(__fdividef(v0, s), __fdividef(v1, s));
+      }
     } else {
       const float r = __frcp_rn(s);
       const uint64_t r2 = pk2(r, r), ns2 = pk2(-s, -s);
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
       sval = unit_or(sl.valid ? (e << (8u * gj)) : 0u, lg);
       sp = sl.unit_valid && local == 0u;
     } else {
-      sval = kFmt == 0 ? f2u(s) : (e << 23);
+      sval = kPow2 ? (e << 23) : f2u(s);
       sp = sl.valid && kk == 0u;
     }
     st_32_if(sp, static_cast<uint32_t*>(p.s) + sl.sidx, sval);

@@ -133,7 +133,15 @@ enum {
   /* vLLM semantics for UE8M0 scales: s = max(s, 1e-10) before rounding up to a power of
    * two (vLLM PR #41326, test ..._packed_all_zero docstring: an all-zero group then gets
    * exponent byte 0x5E).  No effect on PTGQ_SCALE_FP32. */
-  PTGQ_FLAG_UE8M0_SCALE_FLOOR = 2
+  PTGQ_FLAG_UE8M0_SCALE_FLOOR = 2,
+  /* Compatibility with builds compiled with fast math (SGLang PR #34257, "Implementation
+   * notes": with --use_fast_math the division by the scale rounds differently, and SGLang
+   * PR #30924, "Risks": about 0.2% of int8 codes differ by one from such a build).  Each
+   * element quotient x / s is taken with CUDA's approximate division __fdividef (at most
+   * 2 ulp from the IEEE quotient for the scales that occur here) instead of IEEE division.
+   * Scales are unchanged.  Affects only PTGQ_SCALE_FP32: the UE8M0 quotient is an exact
+   * multiply by a power of two, so the flag has no effect there. */
+  PTGQ_FLAG_FAST_DIVIDE = 4
 };
 
 /* ptgq_quant with option flags (a bitwise OR of PTGQ_FLAG_*); flags == 0 is ptgq_quant. */

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.oracle_quant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i32, vp, i32, i32, i32, vp,
                                        f32, i32]
             L.oracle_quant.restype = i32
+            L.oracle_quant_quotient_bound.argtypes = L.oracle_quant.argtypes + [i32]
+            L.oracle_quant_quotient_bound.restype = i32
             L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
             L.oracle_e4m3_decode.restype = f32
             L.oracle_per_token_quant.argtypes = [vp, i32, i64, i64, vp, vp]
@@ -86,8 +88,12 @@ def _ptr(a):
 def quant(x_bits: np.ndarray, in_dtype: int, n: int, tokens_pad: int, hidden: int,
           group_size: int, out_q: np.ndarray, out_dtype: int, out_s: np.ndarray,
           scale_fmt: int, scale_layout: int, fuse_silu: int, masked_m: np.ndarray | None,
-          eps: float, flags: int = 0) -> None:
+          eps: float, flags: int = 0, quot_ulps: int = 0) -> None:
     """Run the oracle in place on numpy buffers (x as uint16 bit patterns).
+
+    ``quot_ulps`` != 0 makes every code the encoding of a bound on the quotient, ``quot_ulps``
+    binary32 ulps above (> 0) or below (< 0) the exact x / s, rounded outward; the scales are
+    those of the operation itself.
 
     ``out_q`` (uint8) and ``out_s`` (float32, or uint32 for the packed format)
     keep whatever the caller put there wherever the method writes nothing.
@@ -98,9 +104,12 @@ def quant(x_bits: np.ndarray, in_dtype: int, n: int, tokens_pad: int, hidden: in
     mm = None
     if masked_m is not None:
         mm = np.ascontiguousarray(masked_m, dtype=np.int32)
-    rc = lib().oracle_quant(_ptr(x_bits), in_dtype, n, tokens_pad, hidden, group_size,
-                            _ptr(out_q), out_dtype, _ptr(out_s), scale_fmt, scale_layout,
-                            fuse_silu, _ptr(mm), float(eps), flags)
+    args = (_ptr(x_bits), in_dtype, n, tokens_pad, hidden, group_size, _ptr(out_q), out_dtype,
+            _ptr(out_s), scale_fmt, scale_layout, fuse_silu, _ptr(mm), float(eps), flags)
+    if quot_ulps:
+        rc = lib().oracle_quant_quotient_bound(*args, int(quot_ulps))
+    else:
+        rc = lib().oracle_quant(*args)
     if rc != 0:
         raise ValueError(f"oracle_quant rejected its arguments (rc={rc})")
 

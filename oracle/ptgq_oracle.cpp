@@ -179,6 +179,26 @@ bool valid_args(int in_dtype, int64_t n, int64_t tokens_pad, int64_t hidden, int
   return true;
 }
 
+// A binary32 bound on a quotient known only to within k ulps of the exact x / s:
+// with e = x / s evaluated in binary64 (exact to 2^-53 relative for binary32
+// operands, far below one binary32 ulp) and u the binary32 ulp at |e| (2^-149 at
+// zero and for subnormals), the bound is e + k*u rounded outward to binary32 (up
+// for k > 0, down for k < 0).  The encoders are monotone, so a code between the
+// encodings of the two bounds is consistent with such a division.  Used to check
+// the fast-math compatibility mode, whose division has a documented error of at
+// most 2 ulps (CUDA Math API, single-precision intrinsics, __fdividef).
+float quotient_bound(float x, float s, int k) {
+  const double e = static_cast<double>(x) / static_cast<double>(s);
+  int ex = e == 0.0 ? -149 : std::ilogb(e);
+  if (ex < -126) ex = -126;
+  const double u = std::ldexp(1.0, ex - 23);
+  const double b = e + k * u;
+  float f = static_cast<float>(b);
+  if (k > 0 && static_cast<double>(f) < b) f = std::nextafter(f, INFINITY);
+  if (k < 0 && static_cast<double>(f) > b) f = std::nextafter(f, -INFINITY);
+  return f;
+}
+
 }  // namespace
 
 extern "C" {
@@ -215,10 +235,15 @@ int64_t oracle_scale_elems(int64_t n, int64_t tokens_pad, int64_t hidden, int gr
 //   flags    : FLAG_UE8M0_SCALE_FLOOR applies the extra max(s, 1e-10) of the
 //              vLLM kernel before UE8M0 rounding ([vllm#41326], test
 //              ..._packed_all_zero docstring).  0 otherwise.
+//   quot_ulps: 0 for the operation itself.  Non-zero: each code is the encoding of a
+//              bound on the quotient instead of the quotient, for checking a
+//              division that is only known to lie within |quot_ulps| binary32 ulps
+//              of the exact x / s (see quotient_bound).  Scales are unchanged.
 // Returns 0, or -1 for invalid arguments.
-int oracle_quant(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens_pad, int64_t hidden,
-                 int group_size, uint8_t* out_q, int out_dtype, void* out_s, int scale_fmt,
-                 int scale_layout, int fuse_silu, const int32_t* masked_m, float eps, int flags) {
+static int quant_impl(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens_pad,
+                      int64_t hidden, int group_size, uint8_t* out_q, int out_dtype, void* out_s,
+                      int scale_fmt, int scale_layout, int fuse_silu, const int32_t* masked_m,
+                      float eps, int flags, int quot_ulps) {
   if (!valid_args(in_dtype, n, tokens_pad, hidden, group_size, out_dtype, scale_fmt, scale_layout,
                   fuse_silu))
     return -1;
@@ -278,7 +303,8 @@ int oracle_quant(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens_pad,
         uint8_t* qg = qb + r * H + g * G;
         for (int64_t i = 0; i < G; ++i) {
           const float y = v[i] / scale;
-          qg[i] = out_dtype == OUT_E4M3 ? e4m3_encode(y) : static_cast<uint8_t>(int8_encode(y));
+          const float yb = quot_ulps == 0 ? y : quotient_bound(v[i], scale, quot_ulps);
+          qg[i] = out_dtype == OUT_E4M3 ? e4m3_encode(yb) : static_cast<uint8_t>(int8_encode(yb));
         }
         // 5. scale store
         if (scale_fmt == FMT_UE8M0_PACKED) {
@@ -309,6 +335,22 @@ int oracle_quant(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens_pad,
     }
   }
   return 0;
+}
+
+int oracle_quant(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens_pad, int64_t hidden,
+                 int group_size, uint8_t* out_q, int out_dtype, void* out_s, int scale_fmt,
+                 int scale_layout, int fuse_silu, const int32_t* masked_m, float eps, int flags) {
+  return quant_impl(x, in_dtype, n, tokens_pad, hidden, group_size, out_q, out_dtype, out_s,
+                    scale_fmt, scale_layout, fuse_silu, masked_m, eps, flags, 0);
+}
+
+// oracle_quant with each code taken from a quotient bound (quot_ulps != 0).
+int oracle_quant_quotient_bound(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens_pad,
+                                int64_t hidden, int group_size, uint8_t* out_q, int out_dtype,
+                                void* out_s, int scale_fmt, int scale_layout, int fuse_silu,
+                                const int32_t* masked_m, float eps, int flags, int quot_ulps) {
+  return quant_impl(x, in_dtype, n, tokens_pad, hidden, group_size, out_q, out_dtype, out_s,
+                    scale_fmt, scale_layout, fuse_silu, masked_m, eps, flags, quot_ulps);
 }
 
 // Per-token (whole-row) FP8 quantization ([sglang#34257], "Key source snippets": the

@@ -81,7 +81,9 @@ def run_gpu(x: torch.Tensor, c: Case, masked_m=None, stream=None):
     return qh[GUARD:GUARD + qn].copy(), sh[GUARD:GUARD + 4 * sn].view(np.uint32).copy()
 
 
-def run_oracle(x: torch.Tensor, c: Case, masked_m=None):
+def run_oracle(x: torch.Tensor, c: Case, masked_m=None, quot_ulps: int = 0):
+    """The oracle on the same input; ``quot_ulps`` != 0 gives the codes of the quotient bounds
+    instead (see oracle.quant)."""
     masked = masked_m is not None
     n, rows, tokens_pad, H, qn, sn = shapes(x, c, masked)
     q = np.full(qn, SENT_Q[c.out_dtype], dtype=np.uint8)
@@ -92,7 +94,7 @@ def run_oracle(x: torch.Tensor, c: Case, masked_m=None):
     flags = O.FLAG_UE8M0_SCALE_FLOOR if c.flags & P.FLAG_UE8M0_SCALE_FLOOR else 0
     O.quant(synth.bits_u16(x), in_dtype, n, tokens_pad, H, c.group, q, c.out_dtype, sarg,
             c.scale_fmt, c.layout, int(c.silu), None if masked_m is None else np.asarray(masked_m),
-            c.eps, flags)
+            c.eps, flags, quot_ulps)
     return q, s
 
 

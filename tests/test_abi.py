@@ -38,8 +38,9 @@ def test_header_constants_match_binding():
     assert (val("PTGQ_SCALE_FP32"), val("PTGQ_SCALE_UE8M0_PACKED"),
             val("PTGQ_SCALE_UE8M0_FP32")) == (P.SCALE_FP32, P.SCALE_UE8M0_PACKED, P.SCALE_UE8M0_FP32)
     assert (val("PTGQ_ROW_MAJOR"), val("PTGQ_COL_MAJOR_TMA")) == (P.ROW_MAJOR, P.COL_MAJOR_TMA)
-    assert (val("PTGQ_FLAG_NO_PDL"), val("PTGQ_FLAG_UE8M0_SCALE_FLOOR")) == (
-        P.FLAG_NO_PDL, P.FLAG_UE8M0_SCALE_FLOOR)
+    assert (val("PTGQ_FLAG_NO_PDL"), val("PTGQ_FLAG_UE8M0_SCALE_FLOOR"),
+            val("PTGQ_FLAG_FAST_DIVIDE")) == (P.FLAG_NO_PDL, P.FLAG_UE8M0_SCALE_FLOOR,
+                                              P.FLAG_FAST_DIVIDE)
 
 
 def test_strerror_covers_every_status(L):
@@ -86,7 +87,7 @@ def test_validation_codes(L):
     for eps in (0.0, -1.0, 1e-30, float("inf"), float("nan")):
         assert _call(L, eps=eps) == -10
     assert _call(L, silu=2) == -11
-    assert _call(L, flags=4) == -11
+    assert _call(L, flags=8) == -11
     assert _call(L, x=0) == -1
     assert _call(L, q=0) == -1
     assert _call(L, s=0) == -1
