@@ -165,38 +165,76 @@ def aggregate(bytes_per_step: int, steps: int, world: int, max_elapsed_s: float)
 
 # ---------------------------------------------------------------- CPU oracle timing
 
-def oracle_rate(x_cpu, rows_per_step: int, steps: int, warmup: int):
-    """Seconds per sample and GB/s of the oracle on `rows_per_step` rows of the workload."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_rate(x_cpu, rows_per_step: int, steps: int, warmup: int, threads: int = 1):
+    """Seconds and GB/s of the oracle on `rows_per_step` rows of the workload.  With
+    threads > 1 the rows are split into that many blocks of whole rows, each quantized by
+    its own oracle call on its own thread (the calls release the GIL), as independent
+    problems with their own scale buffers; the oracle itself is unchanged."""
     import numpy as np
     import oracle as O
     from fp8_token_group_gb300 import synth
-    sub = x_cpu[:rows_per_step].contiguous()
-    bits = synth.bits_u16(sub)
-    q = np.empty(rows_per_step * H, np.uint8)
-    s = np.empty(O.scale_elems(rows_per_step, 0, H, G, O.FMT_UE8M0_PACKED, O.LAYOUT_COL, 0),
-                 np.uint32)
-    run = lambda: O.quant(bits, O.IN_BF16, rows_per_step, 0, H, G, q, O.OUT_E4M3, s,
-                          O.FMT_UE8M0_PACKED, O.LAYOUT_COL, 0, None, 1e-10)
-    for _ in range(warmup):
-        run()
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        run()
-    el = time.perf_counter() - t0
-    nbytes = algorithmic_bytes(rows_per_step) * steps
+    nb = max(1, min(threads, rows_per_step))
+    edges = [rows_per_step * i // nb for i in range(nb + 1)]
+    blocks = []
+    for i in range(nb):
+        r = edges[i + 1] - edges[i]
+        if r == 0:
+            continue
+        bits = synth.bits_u16(x_cpu[edges[i]:edges[i + 1]].contiguous())
+        q = np.empty(r * H, np.uint8)
+        s = np.empty(O.scale_elems(r, 0, H, G, O.FMT_UE8M0_PACKED, O.LAYOUT_COL, 0), np.uint32)
+        blocks.append((bits, r, q, s))
+
+    def one(b):
+        bits, r, q, s = b
+        O.quant(bits, O.IN_BF16, r, 0, H, G, q, O.OUT_E4M3, s, O.FMT_UE8M0_PACKED,
+                O.LAYOUT_COL, 0, None, 1e-10)
+
+    pool = None
+    if len(blocks) > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        pool = ThreadPoolExecutor(len(blocks))
+        run = lambda: list(pool.map(one, blocks))
+    else:
+        run = lambda: one(blocks[0])
+    try:
+        for _ in range(warmup):
+            run()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            run()
+        el = time.perf_counter() - t0
+    finally:
+        if pool is not None:
+            pool.shutdown()
+    nbytes = sum(algorithmic_bytes(b[1]) for b in blocks) * steps
     return el, nbytes / el / 1e9
 
 
-def cpu_baseline(x_cpu, budget_s: float = 10.0) -> dict:
+def cpu_baseline(x_cpu, budget_s: float = 8.0) -> dict:
+    """The oracle on the host: all cores (one row block per thread), and one core."""
     import oracle as O
     O.build()
-    rows = 64
-    el, _ = oracle_rate(x_cpu, rows, 1, 1)
-    reps = max(1, int(budget_s / max(el, 1e-6)))
-    el, gbs = oracle_rate(x_cpu, rows, reps, 0)
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} rows x {H} of the benchmarked input, {reps} repetitions "
-                      f"({el:.1f} s), single-threaded C++ oracle"}
+    cores = host_cores()
+    rows1, rowsn = 64, 64 * cores
+    el, _ = oracle_rate(x_cpu, rows1, 1, 1)
+    reps1 = max(1, int(budget_s / max(el, 1e-6)))
+    el1, gbs1 = oracle_rate(x_cpu, rows1, reps1, 0)
+    el, _ = oracle_rate(x_cpu, rowsn, 1, 1, threads=cores)
+    repsn = max(1, int(budget_s / max(el, 1e-6)))
+    eln, gbsn = oracle_rate(x_cpu, rowsn, repsn, 0, threads=cores)
+    return {"value": round(gbsn, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "single_core_value": round(gbs1, 4),
+            "sample": f"{rowsn} rows x {H} of the benchmarked input in {cores} row blocks on "
+                      f"{cores} threads, {repsn} repetitions ({eln:.1f} s); one core: {rows1} "
+                      f"rows, {reps1} repetitions ({el1:.1f} s); C++ oracle"}
 
 
 def run_reference(args, world, rank):
@@ -207,18 +245,20 @@ def run_reference(args, world, rank):
     O.build()
     x = synth.flat_outliers()
     # size each step so the whole run stays within about a minute
-    el1, _ = oracle_rate(x, 1, 2, 1)
-    per_row = el1 / 2
-    rows = int(max(1, min(T, 60.0 / max(args.steps + args.warmup, 1) / max(per_row, 1e-7))))
-    el, gbs = oracle_rate(x, rows, args.steps, args.warmup)
+    cores = host_cores()
+    el1, _ = oracle_rate(x, cores, 2, 1, threads=cores)
+    per_row = el1 / 2 / cores              # wall seconds per row with all cores busy
+    rows = int(max(cores, min(T, 60.0 / max(args.steps + args.warmup, 1) / max(per_row, 1e-7))))
+    el, gbs = oracle_rate(x, rows, args.steps, args.warmup, threads=cores)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{rows} rows x {H} per step, single-threaded C++ oracle"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows x {H} per step in {cores} row blocks on "
+                                   f"{cores} threads, C++ oracle"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -234,9 +274,11 @@ L2_BYTES = 129 * 2 ** 20
 class Workload:
     """One configuration: seeded CPU input, quantization arguments, algorithmic bytes."""
 
-    def __init__(self, name, desc, make, *, silu=False, fmt=0, layout=0, group=G, out=0):
+    def __init__(self, name, desc, make, *, silu=False, fmt=0, layout=0, group=G, out=0,
+                 expected_m=0):
         self.name, self.desc, self.make = name, desc, make
         self.silu, self.fmt, self.layout, self.group, self.out = silu, fmt, layout, group, out
+        self.expected_m = expected_m
 
     def inputs(self):
         r = self.make()
@@ -262,7 +304,8 @@ class Workload:
 
     def call(self, P, xd, q, s, mm=None):
         P.quant(xd, q, s, self.group, out_dtype=self.out, scale_fmt=self.fmt,
-                scale_layout=self.layout, fuse_silu=self.silu, masked_m=mm)
+                scale_layout=self.layout, fuse_silu=self.silu, masked_m=mm,
+                expected_m=self.expected_m)
 
     def alloc(self, P, xd, mm):
         return P.alloc_outputs(xd, self.group, out_dtype=self.out, scale_fmt=self.fmt,
@@ -346,6 +389,13 @@ def workloads():
         "masked_silu": Workload("masked_silu", "masked EP-MoE bf16 [32,384,2x4096], masked_m "
                                 "uniform in [0,384], fused silu, G=128, e4m3, UE8M0 packed "
                                 "column-major", synth.masked_silu, silu=True, fmt=1, layout=1),
+        "masked_decode": Workload("masked_decode", "masked EP-MoE decode: bf16 [32,384,2x4096] "
+                                  "buffer, 1 live row per expert (masked_m = 1), fused silu, "
+                                  "G=128, e4m3, UE8M0 packed column-major, no expected_m hint",
+                                  synth.masked_decode, silu=True, fmt=1, layout=1),
+        "masked_decode_hint": Workload("masked_decode_hint", "as masked_decode, with the "
+                                       "expected_m = 1 hint", synth.masked_decode, silu=True,
+                                       fmt=1, layout=1, expected_m=1),
         "sweep_big": Workload("sweep_big", "flat bf16 [32768,7168] N(0,1), G=128, e4m3, fp32 "
                               "row-major", lambda: synth.normal((32768, 7168), torch.bfloat16,
                                                                 seed=1)),
@@ -366,11 +416,49 @@ def build_sets(P, wl, x_cpu, mm_cpu, device):
     while GRAPH_CALLS % nsets:
         nsets += 1
     mm = None if mm_cpu is None else mm_cpu.to(device)
+    if mm is not None and x_cpu.shape[1] > VIEW_SETS_PER_BUFFER and \
+            nsets * x_cpu.numel() * 2 > 8 * 2 ** 30:
+        return build_view_sets(P, wl, x_cpu, mm, device, nsets)
     sets = []
     for _ in range(nsets):
         xd = x_cpu.to(device)
         q, s = wl.alloc(P, xd, mm)
         sets.append((xd, q, s, mm))
+    return sets
+
+
+VIEW_SETS_PER_BUFFER = 200
+
+
+def build_view_sets(P, wl, x_cpu, mm, device, nsets):
+    """Masked sets with few live rows (decode): a full copy of the [E, tokens_pad, .] buffers
+    per set would take hundreds of GB.  Instead set j of a buffer views it from row j on,
+    so expert e's live rows of set j are rows e * tokens_pad + j + [0, masked_m[e]):
+    distinct between sets while j + masked_m[e] <= tokens_pad, which holds for the
+    decode counts this is used with.  The scale view is shifted by j words, which moves
+    the written words of the column-major layout by j rows."""
+    import torch
+    E, tp, hin = x_cpu.shape
+    H = hin // 2 if wl.silu else hin
+    assert int(mm.max()) + VIEW_SETS_PER_BUFFER <= tp
+    nbuf = -(-nsets // VIEW_SETS_PER_BUFFER)
+    ns = P.scale_elems(E, tp, H, wl.group, wl.fmt, wl.layout, True)
+    qdt = torch.int8 if wl.out == 1 else torch.float8_e4m3fn
+    sdt = torch.int32 if wl.fmt == 1 else torch.float32
+    flat = x_cpu.reshape(E * tp, hin)
+    extra = VIEW_SETS_PER_BUFFER
+    sets = []
+    for b in range(nbuf):
+        xb = torch.cat([flat.roll(b * 1009, 0), flat[:extra]]).to(device)
+        qb = torch.empty(((E * tp + extra) * H,), dtype=qdt, device=device)
+        sb = torch.empty((ns + extra,), dtype=sdt, device=device)
+        for j in range(VIEW_SETS_PER_BUFFER):
+            if len(sets) == nsets:
+                break
+            xd = xb[j:j + E * tp].view(E, tp, hin)
+            q = qb[j * H:(j + E * tp) * H].view(E, tp, H)
+            s = sb[j:j + ns]
+            sets.append((xd, q, s, mm))
     return sets
 
 
@@ -475,6 +563,9 @@ def time_e2e_zero_copy(P, wl, x_cpu, mm_cpu, steps: int, device):
     inside the quantization call itself.  Two buffer sets alternate."""
     import torch
     mm = None if mm_cpu is None else mm_cpu.to(device)
+    if mm is not None and x_cpu.shape[1] > VIEW_SETS_PER_BUFFER and \
+            nsets * x_cpu.numel() * 2 > 8 * 2 ** 30:
+        return build_view_sets(P, wl, x_cpu, mm, device, nsets)
     sets = []
     for _ in range(2):
         xh = x_cpu.pin_memory()
@@ -602,7 +693,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat_outliers",
                     choices=["flat_outliers", "flat_small", "silu_flat", "masked_silu",
-                             "sweep_big", "per_token", "requant"], help="workload of the JSON line (default: the "
+                             "masked_decode", "masked_decode_hint", "sweep_big", "per_token",
+                             "requant"], help="workload of the JSON line (default: the "
                     "benchmarked flat_outliers)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")

@@ -71,7 +71,7 @@ def lib() -> ctypes.CDLL:
             L.ptgq_quant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i32, vp, i32, i32, i32, vp,
                                      f32, vp]
             L.ptgq_quant.restype = i32
-            L.ptgq_quant_ex.argtypes = L.ptgq_quant.argtypes + [ctypes.c_uint]
+            L.ptgq_quant_ex.argtypes = L.ptgq_quant.argtypes + [ctypes.c_uint, i64]
             L.ptgq_quant_ex.restype = i32
             L.ptgq_scale_elems.argtypes = [i64, i64, i64, i32, i32, i32, i32,
                                            ctypes.POINTER(i64)]
@@ -135,7 +135,7 @@ def alloc_outputs(x, group_size: int, *, out_dtype: int = E4M3, scale_fmt: int =
 def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
           scale_fmt: int = SCALE_FP32, scale_layout: int = ROW_MAJOR, fuse_silu: bool = False,
           masked_m=None, eps: float = 1e-10, tokens_pad: int = 0, flags: int = 0,
-          stream=None) -> None:
+          expected_m: int = 0, stream=None) -> None:
     """Quantize ``x`` into the caller's ``out_q`` / ``out_s`` on ``stream`` (default: torch's
     current stream).  Tensors must be device-accessible: CUDA tensors, or pinned host tensors,
     which the GPU reads and writes in place over the host link (unified addressing).
@@ -165,14 +165,15 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
     rc = lib().ptgq_quant_ex(
         x.data_ptr(), _in_dtype(x), n, tokens_pad, H, group_size, out_q.data_ptr(), out_dtype,
         out_s.data_ptr(), scale_fmt, scale_layout, int(bool(fuse_silu)),
-        None if masked_m is None else masked_m.data_ptr(), float(eps), handle, flags)
+        None if masked_m is None else masked_m.data_ptr(), float(eps), handle, flags,
+        int(expected_m))
     if rc != 0:
         raise PtgqError(rc)
 
 
 def quantize(x, group_size: int = 128, *, out_dtype: int = E4M3, scale_fmt: int = SCALE_FP32,
              scale_layout: int = ROW_MAJOR, fuse_silu: bool = False, masked_m=None,
-             eps: float = 1e-10, tokens_pad: int = 0, flags: int = 0):
+             eps: float = 1e-10, tokens_pad: int = 0, flags: int = 0, expected_m: int = 0):
     """Allocate outputs and quantize.  A host (CPU) ``x`` is copied to the current CUDA
     device, quantized there, and the outputs are copied back to the host."""
     import torch
@@ -186,7 +187,7 @@ def quantize(x, group_size: int = 128, *, out_dtype: int = E4M3, scale_fmt: int 
                          masked=mm is not None, tokens_pad=tokens_pad)
     quant(xd, q, s, group_size, out_dtype=out_dtype, scale_fmt=scale_fmt,
           scale_layout=scale_layout, fuse_silu=fuse_silu, masked_m=mm, eps=eps,
-          tokens_pad=tokens_pad, flags=flags)
+          tokens_pad=tokens_pad, flags=flags, expected_m=expected_m)
     if host:
         q, s = q.cpu(), s.cpu()
     return q, s

@@ -163,11 +163,12 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
                              int64_t hidden, int group_size, void* out_q, int out_dtype,
                              void* out_s, int scale_fmt, int scale_layout, int fuse_silu,
                              const int32_t* masked_m, float eps, ptgq_stream_t stream,
-                             unsigned flags) {
+                             unsigned flags, int64_t expected_m) {
   Geometry g;
   int rc = validate(x, dtype, n, tokens_pad, hidden, group_size, out_q, out_dtype, out_s,
                     scale_fmt, scale_layout, fuse_silu, masked_m, eps, flags, &g);
   if (rc != PTGQ_OK) return rc;
+  if (expected_m < 0) return PTGQ_ERR_SHAPE;
   const bool masked = masked_m != nullptr;
   if (g.blocks * g.rows == 0) return PTGQ_OK;   // nothing to read or write
 
@@ -212,9 +213,11 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   rc = launch_blocks(fn, dev, smem, &per_sm, &sms);
   if (rc != PTGQ_OK) return rc;
 
-  // Persistent grid: at most one full wave, fewer when the work is small.
+  // Persistent grid: at most one full wave, fewer when the work is small (masked: as
+  // small as the expected live rows need, when the caller gives a hint).
   const int64_t lanes_per_unit = (int64_t(group_size) / 16) << g.ug_log2;
-  const int64_t units_max = (masked ? g.blocks * g.rows : n) * g.upr;
+  const int64_t rows_hint = expected_m > 0 ? std::min<int64_t>(expected_m, g.rows) : g.rows;
+  const int64_t units_max = (masked ? g.blocks * rows_hint : n) * g.upr;
   const int64_t tasks = (units_max * lanes_per_unit + 31) / 32;
   int64_t want = (tasks + kWarps - 1) / kWarps;
   if (!masked) {
@@ -250,7 +253,7 @@ extern "C" int ptgq_quant(const void* x, int dtype, int64_t n, int64_t tokens_pa
                           int scale_layout, int fuse_silu, const int32_t* masked_m, float eps,
                           ptgq_stream_t stream) {
   return ptgq_quant_ex(x, dtype, n, tokens_pad, hidden, group_size, out_q, out_dtype, out_s,
-                       scale_fmt, scale_layout, fuse_silu, masked_m, eps, stream, 0u);
+                       scale_fmt, scale_layout, fuse_silu, masked_m, eps, stream, 0u, 0);
 }
 
 extern "C" int ptgq_scale_elems(int64_t n, int64_t tokens_pad, int64_t hidden, int group_size,

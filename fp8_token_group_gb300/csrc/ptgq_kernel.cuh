@@ -103,8 +103,17 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
   if constexpr (kMasked) {
     masked_prefix(p.masked_m, p.n, p.rows, prefix);
     __syncthreads();
-    bshift = bucket_shift(static_cast<uint32_t>(prefix[p.n]));
-    build_buckets(prefix, static_cast<int>(p.n), static_cast<uint32_t>(prefix[p.n]), bshift, bucket);
+    // A grid sized without knowing the live counts (no hint) often has CTAs with no task:
+    // they return here, before the row-to-expert buckets (the condition is uniform).
+    const uint32_t live = static_cast<uint32_t>(prefix[p.n]);
+    const uint32_t upw_log2 = 5u - (p.lg_log2 + p.ug_log2);
+    const uint32_t tasks = (live * p.upr + (1u << upw_log2) - 1u) >> upw_log2;
+    if (blockIdx.x * kWarps >= tasks) {
+      if constexpr (kSilu) copy_to_smem_wait();    // no copy outlives its CTA
+      return;
+    }
+    bshift = bucket_shift(live);
+    build_buckets(prefix, static_cast<int>(p.n), live, bshift, bucket);
   }
   if constexpr (kSilu) copy_to_smem_wait();
   __syncthreads();

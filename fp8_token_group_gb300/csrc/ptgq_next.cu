@@ -75,22 +75,14 @@ __device__ __forceinline__ void quantize16(const uint32_t (&w)[4], float inv, ui
   }
 }
 
-// Rows staged in shared memory.  A warp owns one row at a time and kBufs row buffers; the
-// copies of its next kBufs-1 rows (cp.async, 16 bytes per lane per instruction) are in
-// flight while the warp reduces and quantizes the current row, so each row is read from
-// HBM once.  A lane copies and later reads only its own 16-byte chunks, so the only
-// cross-lane step is the max reduction.  Rows must be a multiple of 16 bytes; the launcher
-// sizes the CTA (32 to 256 threads) so that kBufs buffers per warp fit in shared memory.
-#ifndef PTGQ_PT_BUFS
-#define PTGQ_PT_BUFS 2
-#endif
-#ifndef PTGQ_PT_WARPS
-#define PTGQ_PT_WARPS 8
-#endif
-constexpr int kPtBufs = PTGQ_PT_BUFS;        // row buffers per warp
-constexpr int kPtWarps = PTGQ_PT_WARPS;      // most warps per CTA
-
-template <int kIn>
+// Rows staged in shared memory.  A warp owns one row at a time and kPtBufs row buffers:
+// 2 when it takes several rows (the copy of its next row, cp.async with 16 bytes per lane
+// per instruction, is in flight while it reduces and quantizes the current one), 1 when
+// every warp takes at most one row.  Each row is read from HBM once.  A lane copies and
+// later reads only its own 16-byte chunks, so the only cross-lane step is the max
+// reduction.  Rows must be a multiple of 16 bytes; the launcher picks the CTA size (1 to 8
+// warps) and the buffer count (per_token_shape).
+template <int kIn, int kPtBufs>
 __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerTokenParams p) {
   extern __shared__ __align__(16) unsigned char rowbuf[];
   constexpr int kEsize = kIn == 2 ? 4 : 2;
@@ -301,7 +293,9 @@ std::map<std::tuple<const void*, int, size_t>, int> g_occ;   // (kernel, device,
 std::map<int, int> g_sms;
 std::map<std::pair<const void*, int>, size_t> g_smem_attr;   // (kernel, device) -> attribute set
 
-int grid_for(const void* fn, size_t smem, int64_t want, int threads = kThreads) {
+// Resident CTAs per SM of `fn` at this shared-memory size and CTA size (raising the
+// kernel's dynamic shared-memory limit first when needed), and the SM count.  0 or -1.
+int occupancy(const void* fn, size_t smem, int threads, int* blocks_per_sm, int* sm_count) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -336,7 +330,15 @@ int grid_for(const void* fn, size_t smem, int64_t want, int threads = kThreads) 
     }
     o = g_occ.emplace(std::make_tuple(fn, dev, smem + static_cast<size_t>(threads) * 1000000u), nb).first;
   }
-  const int64_t full = static_cast<int64_t>(o->second) * s->second;
+  *blocks_per_sm = o->second;
+  *sm_count = s->second;
+  return 0;
+}
+
+int grid_for(const void* fn, size_t smem, int64_t want, int threads = kThreads) {
+  int bps = 0, sms = 0;
+  if (occupancy(fn, smem, threads, &bps, &sms) != 0) return -1;
+  const int64_t full = static_cast<int64_t>(bps) * sms;
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, full)));
 }
 
@@ -372,12 +374,66 @@ const void* per_token_reg_fn(int dtype, bool wide) {
   }
 }
 
-const void* per_token_smem_fn(int dtype) {
-  switch (dtype) {
-    case 0: return reinterpret_cast<const void*>(&per_token_smem_kernel<0>);
-    case 1: return reinterpret_cast<const void*>(&per_token_smem_kernel<1>);
-    default: return reinterpret_cast<const void*>(&per_token_smem_kernel<2>);
+const void* per_token_smem_fn(int dtype, int bufs) {
+  switch (dtype * 2 + (bufs == 2 ? 1 : 0)) {
+    case 0: return reinterpret_cast<const void*>(&per_token_smem_kernel<0, 1>);
+    case 1: return reinterpret_cast<const void*>(&per_token_smem_kernel<0, 2>);
+    case 2: return reinterpret_cast<const void*>(&per_token_smem_kernel<1, 1>);
+    case 3: return reinterpret_cast<const void*>(&per_token_smem_kernel<1, 2>);
+    case 4: return reinterpret_cast<const void*>(&per_token_smem_kernel<2, 1>);
+    default: return reinterpret_cast<const void*>(&per_token_smem_kernel<2, 2>);
   }
+}
+
+// Shape of the staged per-token launch: warps per CTA, row buffers per warp, CTAs.
+struct PtShape {
+  int warps = 0, bufs = 0, grid = 0;
+  size_t smem = 0;
+  const void* fn = nullptr;
+};
+
+// Rows are whole work units (a row's max must be known before any of its codes), so the
+// last round of rows leaves warps idle unless the warps divide the rows evenly.  Each SM
+// streams its resident warps' rows at its share of HBM bandwidth, so the time is about
+// rounds * (warps per SM), with the CTAs of the grid spread evenly over the SMs; the shape
+// minimizing that product wins, ties going to more warps in total.  One buffer per warp
+// is allowed only when every warp takes at most one row (nothing to overlap).  Returns
+// false when no shape fits.  PTGQ_PT_FORCE_BUFS / _WARPS restrict the choice (sweeps).
+bool per_token_shape(int dtype, int64_t tokens, int64_t row_bytes, PtShape* out) {
+  constexpr int64_t kMaxSmem = 227 * 1024;
+  int64_t best_cost = -1, best_total = 0;
+  for (int bufs = 2; bufs >= 1; --bufs) {
+#ifdef PTGQ_PT_FORCE_BUFS
+    if (bufs != PTGQ_PT_FORCE_BUFS) continue;
+#endif
+    const void* fn = per_token_smem_fn(dtype, bufs);
+    for (int wc = 1; wc <= kWarps; ++wc) {
+#ifdef PTGQ_PT_FORCE_WARPS
+      if (wc != PTGQ_PT_FORCE_WARPS) continue;
+#endif
+      const int64_t smem = static_cast<int64_t>(wc) * bufs * row_bytes;
+      if (smem > kMaxSmem) break;
+      int bps = 0, sms = 0;
+      if (occupancy(fn, static_cast<size_t>(smem), 32 * wc, &bps, &sms) != 0 || bps < 1)
+        continue;                                   // this shape does not fit
+      const int64_t total = static_cast<int64_t>(sms) * bps * wc;
+      const int64_t rounds = (tokens + total - 1) / total;
+      if (bufs == 1 && rounds > 1) continue;
+      const int64_t grid = std::min<int64_t>(static_cast<int64_t>(sms) * bps, (tokens + wc - 1) / wc);
+      const int64_t used = grid * wc;
+      const int64_t cost = rounds * ((grid + sms - 1) / sms) * wc;
+      if (best_cost < 0 || cost < best_cost || (cost == best_cost && used > best_total)) {
+        best_cost = cost;
+        best_total = used;
+        out->warps = wc;
+        out->bufs = bufs;
+        out->smem = static_cast<size_t>(smem);
+        out->fn = fn;
+        out->grid = static_cast<int>(grid);
+      }
+    }
+  }
+  return best_cost >= 0;
 }
 
 }  // namespace
@@ -403,19 +459,14 @@ extern "C" int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens
     return PTGQ_ERR_ALIGN;
   PerTokenParams p{x, static_cast<uint8_t*>(out_q), out_s, num_tokens, hidden};
   void* args[] = {&p};
-  // Staged kernel: rows that are a multiple of 16 bytes and of which kPtBufs fit per warp
-  // in a 200 KB shared-memory budget with at least two warps per CTA.
+  // Staged kernel: rows that are a multiple of 16 bytes, at least 512 bytes long, and of
+  // which two fit in a CTA's shared memory.
   const int64_t row_bytes = hidden * esize;
-  constexpr int64_t kSmemBudget = 200 * 1024;
-  const int64_t warps_fit = kSmemBudget / (kPtBufs * row_bytes);
-  if (row_bytes % 16 == 0 && row_bytes >= 512 && warps_fit >= 2 &&
+  if (row_bytes % 16 == 0 && row_bytes >= 512 && 2 * row_bytes <= 227 * 1024 &&
       reinterpret_cast<uintptr_t>(x) % 16 == 0) {
-    const int warps = static_cast<int>(std::min<int64_t>(kPtWarps, warps_fit));
-    const size_t smem = static_cast<size_t>(warps) * kPtBufs * static_cast<size_t>(row_bytes);
-    const void* fn = per_token_smem_fn(dtype);
-    const int grid = grid_for(fn, smem, (num_tokens + warps - 1) / warps, 32 * warps);
-    if (grid < 0) return PTGQ_ERR_CUDA;
-    return launch(fn, grid, smem, stream, args, 32 * warps);
+    PtShape sh;
+    if (!per_token_shape(dtype, num_tokens, row_bytes, &sh)) return PTGQ_ERR_CUDA;
+    return launch(sh.fn, sh.grid, sh.smem, stream, args, 32 * sh.warps);
   }
   const void* fn = per_token_reg_fn(dtype, wide);
   const int grid = grid_for(fn, 0, (num_tokens + kWarps - 1) / kWarps);

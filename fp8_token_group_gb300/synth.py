@@ -77,6 +77,14 @@ SWEEP_GROUPS = (16, 32, 64, 128)
 SWEEP_OUTS = ("e4m3", "int8")
 
 
+def masked_decode(experts: int = 32, tokens_pad: int = 384, hidden: int = 4096, live: int = 1,
+                  dtype=torch.bfloat16):
+    """Decode-sized masked batch: the [E, tokens_pad, 2*hidden] buffer of the masked
+    workload with `live` rows in every expert."""
+    x = normal((experts, tokens_pad, 2 * hidden), dtype, seed=0)
+    return x, torch.full((experts,), live, dtype=torch.int32)
+
+
 def sweep_cases():
     """All (index, tokens, hidden, dtype, group, out) tuples of the shape sweep."""
     prod = itertools.product(SWEEP_TOKENS, SWEEP_HIDDEN, SWEEP_DTYPES, SWEEP_GROUPS, SWEEP_OUTS)

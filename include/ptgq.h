@@ -144,11 +144,20 @@ enum {
   PTGQ_FLAG_FAST_DIVIDE = 4
 };
 
-/* ptgq_quant with option flags (a bitwise OR of PTGQ_FLAG_*); flags == 0 is ptgq_quant. */
+/* ptgq_quant with option flags (a bitwise OR of PTGQ_FLAG_*) and a hint;
+ * flags == 0 and expected_m == 0 is ptgq_quant.
+ *   expected_m  masked mode: the caller's estimate of the live rows per expert (sglang PR
+ *               #30924, "Implementation breakdown" item 2: the custom op takes masked_m
+ *               and expected_m).  The live counts sit in device memory, so without a hint
+ *               the grid is sized for every row of tokens_pad being live; with one it is
+ *               sized for E * min(expected_m, tokens_pad) rows.  Results are the same for
+ *               any value: the grid strides over whatever rows are live, so a low hint
+ *               costs time, never correctness.  0: no hint.  Ignored in flat mode.
+ *               Negative: PTGQ_ERR_SHAPE. */
 int ptgq_quant_ex(const void* x, int dtype, int64_t num_tokens_or_E, int64_t tokens_pad,
                   int64_t hidden, int group_size, void* out_q, int out_dtype, void* out_s,
                   int scale_fmt, int scale_layout, int fuse_silu, const int32_t* masked_m,
-                  float eps, ptgq_stream_t stream, unsigned flags);
+                  float eps, ptgq_stream_t stream, unsigned flags, int64_t expected_m);
 
 /* Size helper: the number of scale elements (floats, or int32 words for the packed format)
  * that out_s must hold for these arguments (masked != 0 selects the masked layout, where

@@ -32,6 +32,7 @@ class Case:
     tokens_pad: int = 0
     eps: float = 1e-10
     flags: int = 0
+    expected_m: int = 0
 
 
 def _guarded(nbytes: int, fill: int, device="cuda"):
@@ -73,7 +74,7 @@ def run_gpu(x: torch.Tensor, c: Case, masked_m=None, stream=None):
     st = sbody.view(torch.int32 if c.scale_fmt == P.SCALE_UE8M0_PACKED else torch.float32)
     P.quant(xd, qt, st, c.group, out_dtype=c.out_dtype, scale_fmt=c.scale_fmt,
             scale_layout=c.layout, fuse_silu=c.silu, masked_m=mm, eps=c.eps,
-            tokens_pad=tokens_pad, flags=c.flags, stream=stream)
+            tokens_pad=tokens_pad, flags=c.flags, expected_m=c.expected_m, stream=stream)
     torch.cuda.synchronize()
     qh, sh = qbuf.cpu().numpy(), sbuf.cpu().numpy()
     assert np.all(qh[:GUARD] == CANARY) and np.all(qh[GUARD + qn:] == CANARY), "out_q guard hit"

@@ -104,6 +104,24 @@ def test_masked_scheduler_grid(E, H, tp):
             masked_m=mm.numpy())
 
 
+@pytest.mark.parametrize("expected_m", [1, 7, 200, 384, 100000])
+def test_masked_expected_m_hint_changes_nothing(expected_m):
+    """A hint far below, near or above the live counts sizes the grid differently; the
+    grid strides over the live rows either way, so every output matches the oracle."""
+    x, mm = synth.masked_silu(experts=32, tokens_pad=384, hidden=2048)
+    compare(x, Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA,
+                    expected_m=expected_m), masked_m=mm.numpy())
+
+
+def test_masked_decode_one_row_per_expert():
+    """Decode-sized masked batch: one live row in each of 32 experts of 384, with and
+    without the matching hint (most CTAs of the hint-less grid find no work and return)."""
+    x, mm = synth.masked_decode()
+    for hint in (0, 1):
+        compare(x, Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA,
+                        expected_m=hint), masked_m=mm.numpy())
+
+
 # ---------------------------------------------------------------- every variant, ragged shapes
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
