@@ -563,9 +563,6 @@ def time_e2e_zero_copy(P, wl, x_cpu, mm_cpu, steps: int, device):
     inside the quantization call itself.  Two buffer sets alternate."""
     import torch
     mm = None if mm_cpu is None else mm_cpu.to(device)
-    if mm is not None and x_cpu.shape[1] > VIEW_SETS_PER_BUFFER and \
-            nsets * x_cpu.numel() * 2 > 8 * 2 ** 30:
-        return build_view_sets(P, wl, x_cpu, mm, device, nsets)
     sets = []
     for _ in range(2):
         xh = x_cpu.pin_memory()
