@@ -21,6 +21,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -54,19 +55,23 @@ struct Slot {
 // Tuning, per instance (compile-time), from sweeps on GB300: tasks per warp batch, whether
 // the next batch's loads are issued before the current batch is computed, and the CTAs per
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
-// CTAs/SM (64 registers).  bf16 silu: flat pipelined at 3 CTAs/SM, masked unpipelined at
-// 4 CTAs/SM.  fp16 silu: pipelined at 2 CTAs/SM (its per-element exponential needs the
-// registers).  PTGQ_TUNE_BATCH / _PIPELINE / _MIN_BLOCKS override all instances (sweeps).
+// CTAs/SM (64 registers).  bf16 silu, 3 CTAs/SM: flat one task pipelined, masked two tasks
+// loaded then computed.  fp16 silu: pipelined at 2 CTAs/SM (its per-element exponential
+// needs the registers).  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE / _MIN_BLOCKS override all
+// instances (sweeps).
+#ifndef PTGQ_TUNE_SILU_BATCH
+#define PTGQ_TUNE_SILU_BATCH 1
+#endif
 template <bool kFp16, bool kSilu, bool kMasked>
 struct Tuning {
 #ifdef PTGQ_TUNE_BATCH
-  static constexpr int batch = kSilu ? 1 : PTGQ_TUNE_BATCH;
+  static constexpr int batch = kSilu ? PTGQ_TUNE_SILU_BATCH : PTGQ_TUNE_BATCH;
   static constexpr bool pipeline = PTGQ_TUNE_PIPELINE;
   static constexpr int min_blocks = PTGQ_TUNE_MIN_BLOCKS;
 #else
-  static constexpr int batch = kSilu ? 1 : 2;
+  static constexpr int batch = (kSilu && (kFp16 || !kMasked)) ? 1 : 2;
   static constexpr bool pipeline = kSilu && (kFp16 || !kMasked);
-  static constexpr int min_blocks = !kSilu ? 4 : (kFp16 ? 2 : (kMasked ? 4 : 3));
+  static constexpr int min_blocks = !kSilu ? 4 : (kFp16 ? 2 : 3);
 #endif
 };
 
@@ -181,24 +186,36 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
           v[i] = mul2(pk2(s0, s1), widen2<true>(b.w[i]));
         }
       } else {
-        // Table index = (|bits| - FIELD_LO*128) per 16-bit half, plus SPAN for a negative
-        // gate.  A gate outside the table range (|g| < 2^-25, including zero, or
-        // |g| >= 256) shows as a half >= SPAN; the first pass finds whether the warp has
-        // any, and only then does the warp take the full definition (silu_bf16).
+        // Table entry (|bits| - FIELD_LO*128), plus SPAN for a negative gate.  Both 16-bit
+        // halves of a word are offset at once: bit 15 of each half is set before the
+        // subtraction (so no borrow crosses halves) and flipped back after it, leaving
+        // t = |bits| - FIELD_LO*128 per half, wrapped to >= 0x8000 for a gate below the
+        // table (|g| < 2^-25, zero included) and >= SPAN = 0x1000 for one above it
+        // (|g| >= 128).  A warp whose OR of all t has no bit at 12 or above in either half
+        // reads only inside the table (byte offsets <= 0x7FFC of 0x8000); otherwise the
+        // warp takes the full definition (silu_bf16).
+        static_assert(PTGQ_SILU_BF16_SPAN == 4096, "the range check assumes SPAN = 2^12");
         constexpr uint32_t kBase = PTGQ_SILU_BF16_FIELD_LO << 7;
         constexpr uint32_t kBase2 = kBase | (kBase << 16);
         constexpr uint32_t kSpan = PTGQ_SILU_BF16_SPAN;
-        uint32_t dmax = 0u;
+        uint32_t t[8];
+        uint32_t acc = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dmax = __vmaxu2(dmax, __vsub2(a.w[i] & 0x7FFF7FFFu, kBase2));
-        const bool oob = max(dmax & 0xFFFFu, dmax >> 16) >= kSpan;
+        for (int i = 0; i < 8; ++i) {
+          t[i] = ((a.w[i] | 0x80008000u) - kBase2) ^ 0x80008000u;
+          acc |= t[i];
+        }
+        const bool oob = (acc & 0xF000F000u) != 0u;
         if (!__any_sync(0xFFFFFFFFu, oob)) {
+          const char* tab = reinterpret_cast<const char*>(silu_tab);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint32_t w = a.w[i];
-            const uint32_t d = __vsub2(w & 0x7FFF7FFFu, kBase2);
-            const float s0 = silu_tab[(d & 0xFFFFu) + ((w >> 15) & 1u) * kSpan];
-            const float s1 = silu_tab[(d >> 16) + (w >> 31) * kSpan];
+            // byte offsets 4*t (positive gate) or 4*(SPAN + t) = 0x4000 + 4*t (negative)
+            const uint32_t o0 = ((t[i] << 2) & 0x3FFCu) | ((w >> 1) & 0x4000u);
+            const uint32_t o1 = ((t[i] >> 14) & 0x3FFCu) | ((w >> 17) & 0x4000u);
+            const float s0 = *reinterpret_cast<const float*>(tab + o0);
+            const float s1 = *reinterpret_cast<const float*>(tab + o1);
             v[i] = mul2(pk2(s0, s1), widen2<false>(b.w[i]));
           }
         } else {
@@ -210,13 +227,16 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
           }
         }
       }
-      amax_bits = 0u;
+      // max |v| as floats (for finite non-negative floats the order of the values is the
+      // order of their bit patterns, so this is the same maximum)
+      float amax_f = 0.0f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float y0, y1;
         upk2(v[i], y0, y1);
-        amax_bits = max(amax_bits, max(f2u(y0) & 0x7FFFFFFFu, f2u(y1) & 0x7FFFFFFFu));
+        amax_f = fmaxf(amax_f, fmaxf(fabsf(y0), fabsf(y1)));
       }
+      amax_bits = f2u(amax_f);
     } else {
       uint32_t m01 = maxabs2<kFp16>(a.w[0], a.w[1]), m23 = maxabs2<kFp16>(a.w[2], a.w[3]);
       uint32_t m45 = maxabs2<kFp16>(a.w[4], a.w[5]), m67 = maxabs2<kFp16>(a.w[6], a.w[7]);
@@ -285,16 +305,24 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked>::min_
     st_32_if(sp, static_cast<uint32_t*>(p.s) + sl.sidx, sval);
   };
 
+  // Batches of KB tasks: all their loads are issued, then all are computed.
+  auto batches = [&](auto kb) {
+    constexpr int KB = decltype(kb)::value;
+    for (uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_tasks; t += KB * stride) {
+      Slot cur[KB];
+      Raw16 ca[KB], cb[KB];
+#pragma unroll
+      for (int i = 0; i < KB; ++i) issue(t + i * stride, cur[i], ca[i], cb[i]);
+#pragma unroll
+      for (int i = 0; i < KB; ++i) finish(cur[i], ca[i], cb[i]);
+    }
+  };
   // Software pipeline: the next batch's loads are in flight while this batch computes.
   if (total_units > 0u && !Tune::pipeline) {
-    for (uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_tasks; t += kB * stride) {
-      Slot cur[kB];
-      Raw16 ca[kB], cb[kB];
-#pragma unroll
-      for (int i = 0; i < kB; ++i) issue(t + i * stride, cur[i], ca[i], cb[i]);
-#pragma unroll
-      for (int i = 0; i < kB; ++i) finish(cur[i], ca[i], cb[i]);
-    }
+    // When no warp has a second task (small or decode-sized work), one-task batches: the
+    // empty slots of a wider batch would still be computed and only lengthen the call.
+    if (kB > 1 && total_tasks <= stride) batches(std::integral_constant<int, 1>{});
+    else batches(std::integral_constant<int, kB>{});
   } else if (total_units > 0u) {
     uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     Slot cur[kB];

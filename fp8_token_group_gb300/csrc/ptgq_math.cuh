@@ -115,9 +115,9 @@ PTGQ_HD float silu_generic(float g, const float2* exp_int, const float2* exp_fra
 }
 
 // The same sequence for a bf16 gate, read from the precomputed table of binary32
-// results for 2^-25 <= |g| < 256; outside that range the sequence has closed
-// forms: S = g/2 for |g| < 2^-25 (E = 1, D = 2), S = g for g >= 256 (E = 0) and
-// S = -0 for g <= -256 (E = +inf).
+// results for 2^-25 <= |g| < 128; outside that range the sequence has closed
+// forms: S = g/2 for |g| < 2^-25 (E = 1, D = 2), S = g for g >= 128 (E = 0) and
+// S = -0 for g <= -128 (E = +inf).
 PTGQ_HD float silu_bf16(uint32_t h, const float* table, uint32_t field_lo, uint32_t span) {
   const float g = u2f(h << 16);
   const uint32_t mag = h & 0x7FFFu;
