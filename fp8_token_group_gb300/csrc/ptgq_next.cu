@@ -37,40 +37,45 @@ struct PerTokenParams {
   int64_t hidden;
 };
 
+// Running max |x| of a row.  binary32: the magnitude bit patterns.  16-bit inputs: both
+// halves of a word at once (max.xorsign.abs; the sign bits it leaves are cleared by
+// abs_bits), which gives the same magnitudes as comparing the patterns.
 template <int kIn>
-__device__ __forceinline__ uint32_t absmax_words(const uint32_t* w, int n) {
-  uint32_t m = 0u;
+__device__ __forceinline__ uint32_t absmax_words(uint32_t m, const uint32_t* w, int n) {
   for (int k = 0; k < n; ++k) {
-    if constexpr (kIn == 2) {
-      m = max(m, w[k] & 0x7FFFFFFFu);
-    } else {
-      const uint32_t h = w[k] & 0x7FFF7FFFu;
-      m = max(m, max(h & 0xFFFFu, h >> 16));
-    }
+    if constexpr (kIn == 2) m = max(m, w[k] & 0x7FFFFFFFu);
+    else m = maxabs2<kIn == 1>(m, w[k]);
   }
   return m;
 }
 
-// |x| of the 16-bit element whose magnitude pattern is m (sign cleared), as binary32 bits.
+// The row's max |x| as binary32 bits, from the running value of absmax_words.
 template <int kIn>
 __device__ __forceinline__ uint32_t abs_bits(uint32_t m) {
-  if constexpr (kIn == 2) return m;
-  else return f2u(kIn == 1 ? widen_lo<true>(m) : widen_lo<false>(m));
+  if constexpr (kIn == 2) {
+    return m;
+  } else {
+    m &= 0x7FFF7FFFu;
+    const uint32_t h = max(m & 0xFFFFu, m >> 16);
+    return f2u(kIn == 1 ? widen_lo<true>(h) : widen_lo<false>(h));
+  }
 }
 
 // 16 bytes of input (8 16-bit or 4 binary32 elements) -> codes, stored at dst.
+// Products x * inv are formed two at a time (mul.rn.f32x2: each rounded like __fmul_rn).
 template <int kIn>
 __device__ __forceinline__ void quantize16(const uint32_t (&w)[4], float inv, uint8_t* dst) {
+  const uint64_t inv2 = pk2(inv, inv);
   if constexpr (kIn == 2) {
-    const uint32_t o = e4m3x4(__fmul_rn(u2f(w[0]), inv), __fmul_rn(u2f(w[1]), inv),
-                              __fmul_rn(u2f(w[2]), inv), __fmul_rn(u2f(w[3]), inv));
+    const uint32_t o = e4m3x2_pair(mul2(pk2(u2f(w[0]), u2f(w[1])), inv2)) |
+                       (e4m3x2_pair(mul2(pk2(u2f(w[2]), u2f(w[3])), inv2)) << 16);
     asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(o) : "memory");
   } else {
     constexpr bool h = kIn == 1;
-    const uint32_t o0 = e4m3x4(__fmul_rn(widen_lo<h>(w[0]), inv), __fmul_rn(widen_hi<h>(w[0]), inv),
-                               __fmul_rn(widen_lo<h>(w[1]), inv), __fmul_rn(widen_hi<h>(w[1]), inv));
-    const uint32_t o1 = e4m3x4(__fmul_rn(widen_lo<h>(w[2]), inv), __fmul_rn(widen_hi<h>(w[2]), inv),
-                               __fmul_rn(widen_lo<h>(w[3]), inv), __fmul_rn(widen_hi<h>(w[3]), inv));
+    const uint32_t o0 = e4m3x2_pair(mul2(widen2<h>(w[0]), inv2)) |
+                        (e4m3x2_pair(mul2(widen2<h>(w[1]), inv2)) << 16);
+    const uint32_t o1 = e4m3x2_pair(mul2(widen2<h>(w[2]), inv2)) |
+                        (e4m3x2_pair(mul2(widen2<h>(w[3]), inv2)) << 16);
     asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(o0), "r"(o1) : "memory");
   }
 }
@@ -124,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerToken
     for (int64_t c = lane; c < chunks; c += 32) {
       uint32_t w[4];
       chunk(slot, c, w);
-      m = max(m, absmax_words<kIn>(w, 4));
+      m = absmax_words<kIn>(m, w, 4);
     }
     m = redux_max(abs_bits<kIn>(m), 0xFFFFFFFFu);
     const float s = __fdiv_rn(u2f(m), 448.0f);
@@ -188,13 +193,13 @@ __global__ void __launch_bounds__(kThreads) per_token_reg_kernel(const PerTokenP
       const int64_t i = lane + 32 * j;
       if (i < nvec) {
         load(row, i, cache[j]);
-        m = max(m, absmax_words<kIn>(cache[j], kWords));
+        m = absmax_words<kIn>(m, cache[j], kWords);
       }
     }
     for (int64_t i = lane + 32 * kCache; i < nvec; i += 32) {
       uint32_t w[kWords];
       load(row, i, w);
-      m = max(m, absmax_words<kIn>(w, kWords));
+      m = absmax_words<kIn>(m, w, kWords);
     }
     m = redux_max(abs_bits<kIn>(m), 0xFFFFFFFFu);
     const float s = __fdiv_rn(u2f(m), 448.0f);
