@@ -682,6 +682,48 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_sweep(args, out_path=None):
+    """Every configuration of the shape sweep (T in {1, 7, 64, 333, 4096, 32768} x H in
+    {128, 2048, 4096, 7168} x {fp16, bf16} x G in {16, 32, 64, 128} x {e4m3, int8}, fp32
+    row-major scales), each timed like the other workloads (graph replay, rotating buffer
+    sets beyond L2).  Prints one JSON line per configuration and a summary line; the large
+    configurations (T >= 4096 and H >= 2048) are the ones held to the HBM roofline."""
+    import torch
+    import fp8_token_group_gb300 as P
+    from fp8_token_group_gb300 import synth
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    P.lib()
+    peak, peak_kind = measured_peak()
+    rows, large = [], []
+    for idx, T, H, dt, G, out in synth.sweep_cases():
+        if args.sweep_min_tokens and T < args.sweep_min_tokens:
+            continue
+        x = synth.sweep_input(idx, T, H, dt)
+        name = f"{T}x{H}-{str(dt)[6:]}-G{G}-{out}"
+        wl = Workload(name, name, lambda x=x: x, group=G, out=0 if out == "e4m3" else 1)
+        r = measure_device(P, wl, device, args.sweep_steps)
+        pct = round(100 * r["gbs"] / peak, 1)
+        line = {"sweep": idx, "tokens": T, "hidden": H, "dtype": str(dt)[6:], "group": G,
+                "out": out, "us_per_call": r["us_per_call"], "gbs": r["gbs"],
+                "pct_of_peak": pct}
+        print(json.dumps(line), flush=True)
+        rows.append(line)
+        if T >= 4096 and H >= 2048:
+            large.append(pct)
+    summary = {"sweep_summary": {"configs": len(rows), "peak_gbs": peak, "peak_source": peak_kind,
+                                 "large_configs": len(large),
+                                 "large_min_pct": min(large) if large else None,
+                                 "large_median_pct": statistics.median(large) if large else None}}
+    print(json.dumps(summary), flush=True)
+    if out_path:
+        with open(out_path, "w") as f:
+            for line in rows:
+                f.write(json.dumps(line) + "\n")
+            f.write(json.dumps(summary) + "\n")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -695,8 +737,15 @@ def main():
                     "benchmarked flat_outliers)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--sweep", action="store_true", help="time every shape-sweep configuration "
+                    "(one JSON line each, then a summary) instead of the benchmark line")
+    ap.add_argument("--sweep-steps", type=int, default=2000)
+    ap.add_argument("--sweep-min-tokens", type=int, default=0)
+    ap.add_argument("--sweep-out", default=None, help="also write the sweep lines to this file")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep:
+        return run_sweep(args, args.sweep_out)
     if args.impl == "reference":
         # the CPU oracle: rank 0 alone runs it, other ranks exit without work
         return run_reference(args, int(os.environ.get("WORLD_SIZE", "1")),

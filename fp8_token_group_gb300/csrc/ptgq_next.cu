@@ -241,12 +241,13 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantParams p
   int32_t* prefix = reinterpret_cast<int32_t*>(smem);
   griddep_wait();
   griddep_launch_dependents();
+  const float oscale = *p.output_scale;                 // in flight during the prefix sum
   const bool masked = p.masked_m != nullptr;
   uint32_t live_rows = static_cast<uint32_t>(p.experts * p.m);
   if (masked) masked_prefix(p.masked_m, p.experts, p.m, prefix);
   __syncthreads();
   if (masked) live_rows = static_cast<uint32_t>(prefix[p.experts]);
-  const float inv = __frcp_rn(*p.output_scale);
+  const float inv = __frcp_rn(oscale);
 
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t lg = 1u << p.lg_log2;
