@@ -21,10 +21,14 @@ const void* kernel_for_bf16_flat(int int8, int fmt, int silu);
 const void* kernel_for_bf16_masked(int int8, int fmt, int silu);
 const void* kernel_for_fp16_flat(int int8, int fmt, int silu);
 const void* kernel_for_fp16_masked(int int8, int fmt, int silu);
+const void* kernel_for_bf16_flat_light(int int8, int fmt);
+const void* kernel_for_fp16_flat_light(int int8, int fmt);
 int table_bytes_bf16(int silu);
 int table_bytes_fp16(int silu);
 
 const void* kernel_for(const KernelKey& k) {
+  if (k.light && !k.masked && !k.silu)
+    return k.fp16 ? kernel_for_fp16_flat_light(k.int8, k.fmt) : kernel_for_bf16_flat_light(k.int8, k.fmt);
   if (k.fp16)
     return k.masked ? kernel_for_fp16_masked(k.int8, k.fmt, k.silu)
                     : kernel_for_fp16_flat(k.int8, k.fmt, k.silu);
@@ -204,7 +208,7 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
 
   // Internal format 3: fp32 scales with approximate element division (fast-math interop).
   const int kfmt = (scale_fmt == PTGQ_SCALE_FP32 && (flags & PTGQ_FLAG_FAST_DIVIDE)) ? 3 : scale_fmt;
-  const KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, kfmt, fuse_silu, masked};
+  KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, kfmt, fuse_silu, masked, 0};
   const void* fn = kernel_for(key);
   const size_t smem = dynamic_smem_bytes(key, masked ? n : 0);
   int dev = 0;
@@ -219,6 +223,14 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   const int64_t rows_hint = expected_m > 0 ? std::min<int64_t>(expected_m, g.rows) : g.rows;
   const int64_t units_max = (masked ? g.blocks * rows_hint : n) * g.upr;
   const int64_t tasks = (units_max * lanes_per_unit + 31) / 32;
+  // Plain flat work of at most about 8 tasks per warp of the standard grid: the light
+  // flavour (one task per batch, more warps per SM) ramps up faster.
+  if (!masked && !fuse_silu && tasks <= 8 * static_cast<int64_t>(per_sm) * sms * kWarps) {
+    key.light = 1;
+    fn = kernel_for(key);
+    rc = launch_blocks(fn, dev, smem, &per_sm, &sms);
+    if (rc != PTGQ_OK) return rc;
+  }
   int64_t want = (tasks + kWarps - 1) / kWarps;
   if (!masked) {
     const int64_t zero_chunks = (p.zero_q_end - p.zero_q_begin) / 16 + p.zero_s_rows * g.ncol;

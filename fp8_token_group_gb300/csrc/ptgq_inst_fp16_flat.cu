@@ -26,6 +26,20 @@ const void* kernel_for_fp16_flat(int int8, int fmt, int silu) {
   return table[(int8 ? 8 : 0) + fmt * 2 + (silu ? 1 : 0)];
 }
 
+const void* kernel_for_fp16_flat_light(int int8, int fmt) {
+  static const void* const table[8] = {
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 0, false, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 1, false, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 2, false, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 3, false, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 0, false, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 1, false, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 2, false, false, true>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 3, false, false, true>),
+  };
+  return table[(int8 ? 4 : 0) + fmt];
+}
+
 int table_bytes_fp16(int silu) { return silu ? SmemTables<true, true>::bytes : 0; }
 
 }  // namespace ptgq

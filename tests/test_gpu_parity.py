@@ -104,6 +104,18 @@ def test_masked_scheduler_grid(E, H, tp):
             masked_m=mm.numpy())
 
 
+@pytest.mark.parametrize("T", [1024, 4096])
+@pytest.mark.parametrize("fmt,layout", [(P.SCALE_FP32, P.ROW_MAJOR), (P.SCALE_UE8M0_PACKED, P.COL_MAJOR_TMA),
+                                        (P.SCALE_UE8M0_FP32, P.COL_MAJOR_TMA)])
+@pytest.mark.parametrize("out", [P.E4M3, P.INT8])
+def test_flat_light_and_standard_flavours(T, fmt, layout, out):
+    """Plain flat calls of at most about 8 tasks per warp run the light flavour (one task per
+    batch, more warps per SM), larger ones the standard flavour; [1024, 7168] and
+    [4096, 7168] fall on either side, in every scale format and output type."""
+    x = synth.flat_outliers(tokens=T, hidden=7168)
+    compare(x, Case(scale_fmt=fmt, layout=layout, out_dtype=out, tokens_pad=T + 3))
+
+
 @pytest.mark.parametrize("expected_m", [1, 7, 200, 384, 100000])
 def test_masked_expected_m_hint_changes_nothing(expected_m):
     """A hint far below, near or above the live counts sizes the grid differently; the
