@@ -65,7 +65,8 @@ struct Slot {
 // The light flavour of the plain flat instances (kLight): one task per batch at 6 CTAs/SM
 // (40 registers, 48 warps per SM).  It ramps up faster when each warp has only a few
 // tasks, and the launcher takes it below about 8 tasks per warp of the standard grid
-// (4096 x 4096, G = 128: 9.8 us against 10.05 us; 4096 x 7168: 15.4 us against 14.7 us).
+// (4096 x 4096, G = 128: 9.8 us against the standard 10.05 us; at 4096 x 7168 the standard
+// flavour is the faster one, 14.7 us against 15.4 us).
 template <bool kFp16, bool kSilu, bool kMasked, bool kLight = false>
 struct Tuning {
   static_assert(!kLight || (!kSilu && !kMasked), "the light flavour is plain flat only");
