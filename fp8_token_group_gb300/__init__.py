@@ -141,10 +141,12 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
     which the GPU reads and writes in place over the host link (unified addressing).
     Arguments follow ``ptgq_quant`` in include/ptgq.h."""
     import torch
-    for name, t in (("x", x), ("out_q", out_q), ("out_s", out_s)):
-        if not (t.is_cuda or t.is_pinned()):
-            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory "
-                             "(use quantize() for pageable host tensors)")
+    all_cuda = x.is_cuda and out_q.is_cuda and out_s.is_cuda
+    if not all_cuda:
+        for name, t in (("x", x), ("out_q", out_q), ("out_s", out_s)):
+            if not (t.is_cuda or t.is_pinned()):
+                raise ValueError(f"{name} must be a CUDA tensor or pinned host memory "
+                                 "(use quantize() for pageable host tensors)")
     if not (x.is_contiguous() and out_q.is_contiguous() and out_s.is_contiguous()):
         raise ValueError("x, out_q and out_s must be contiguous")
     if out_dtype is None:
@@ -159,10 +161,8 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
     else:
         n, hin = x.shape
     H = hin // 2 if fuse_silu else hin
-    if stream is None:
-        stream = torch.cuda.current_stream(x.device if x.is_cuda else None)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    rc = lib().ptgq_quant_ex(
+    handle = _stream_handle(stream, x.get_device() if x.is_cuda else None)
+    rc = (_lib or lib()).ptgq_quant_ex(
         x.data_ptr(), _in_dtype(x), n, tokens_pad, H, group_size, out_q.data_ptr(), out_dtype,
         out_s.data_ptr(), scale_fmt, scale_layout, int(bool(fuse_silu)),
         None if masked_m is None else masked_m.data_ptr(), float(eps), handle, flags,
@@ -194,9 +194,17 @@ def quantize(x, group_size: int = 128, *, out_dtype: int = E4M3, scale_fmt: int 
 
 
 def _stream_handle(stream, device):
+    """The raw cudaStream_t of ``stream`` (a torch stream or an integer handle), or of torch's
+    current stream on ``device`` (an index, a torch device, or None for the current one)."""
     import torch
     if stream is None:
-        stream = torch.cuda.current_stream(device)
+        idx = device.index if isinstance(device, torch.device) else device
+        if idx is None:
+            idx = torch.cuda.current_device()
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            return raw(idx)                # the handle without building a Stream object
+        stream = torch.cuda.current_stream(idx)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
