@@ -274,19 +274,20 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const RequantParams p
     asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p.x + off));
     const float sc = p.x_scale[e * p.se + r * p.sm + static_cast<int64_t>(g) * p.sg];
+    // (v * sc) * inv two codes at a time: mul.rn.f32x2 rounds each product like __fmul_rn
+    const uint64_t sc2 = pk2(sc, sc), inv2 = pk2(inv, inv);
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float v[4];
+      uint32_t c[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t f16x2;
         const uint16_t pair = static_cast<uint16_t>(w[i] >> (16 * h));
         asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
-        v[2 * h] = __fmul_rn(__fmul_rn(widen_lo<true>(f16x2), sc), inv);
-        v[2 * h + 1] = __fmul_rn(__fmul_rn(widen_hi<true>(f16x2), sc), inv);
+        c[h] = e4m3x2_pair(mul2(mul2(widen2<true>(f16x2), sc2), inv2));
       }
-      o[i] = e4m3x4(v[0], v[1], v[2], v[3]);
+      o[i] = c[0] | (c[1] << 16);
     }
     st_128(p.out + off, o[0], o[1], o[2], o[3]);
   }
