@@ -17,7 +17,8 @@
  *     q_i   = saturate(round_to_nearest_even(v_i / scale))   to e4m3fn or int8
  *   All arithmetic is IEEE binary32 with round-to-nearest-even; silu uses the
  *   correctly rounded binary32 exponential.  Codes and scales are bit-identical to
- *   that definition (the library is tested against an independent CPU oracle).
+ *   that definition (the library is tested against an independent CPU oracle), except
+ *   under PTGQ_FLAG_FAST_DIVIDE, which trades the exact quotient for compatibility.
  *
  * Conventions for every entry point:
  *   - Buffer pointers (x, out_q, out_s, masked_m, ...) are addresses the current device
@@ -76,13 +77,15 @@ enum {
   PTGQ_ERR_OUT_DTYPE = -3,  /* unknown output dtype */
   PTGQ_ERR_GROUP = -4,      /* group_size not in {16, 32, 64, 128} (sglang PR #27449, "Notes") */
   PTGQ_ERR_HIDDEN = -5,     /* hidden <= 0 or hidden % group_size != 0 */
-  PTGQ_ERR_SHAPE = -6,      /* negative count, or flat tokens_pad in (0, num_tokens) */
+  PTGQ_ERR_SHAPE = -6,      /* negative count or expected_m, flat tokens_pad in
+                             * (0, num_tokens), or more than 4096 experts (masked) */
   PTGQ_ERR_ALIGN = -7,      /* x not 32-byte, out_q not 16-byte or out_s not 4-byte aligned */
   PTGQ_ERR_SCALE_FMT = -8,  /* unknown scale format */
   PTGQ_ERR_LAYOUT = -9,     /* unknown scale layout */
   PTGQ_ERR_EPS = -10,       /* eps not finite or below PTGQ_EPS_MIN */
   PTGQ_ERR_FLAG = -11,      /* fuse_silu not 0 or 1, or an unknown flag bit */
-  PTGQ_ERR_TOO_LARGE = -12, /* sizes overflow the 63-bit index space */
+  PTGQ_ERR_TOO_LARGE = -12, /* more than 2^31 - 1 work units (live rows times groups, or
+                             * times packed words, per row), or an index beyond 2^62 */
   PTGQ_ERR_CUDA = -13       /* the kernel launch failed */
 };
 
@@ -182,7 +185,7 @@ int ptgq_scale_elems(int64_t num_tokens_or_E, int64_t tokens_pad, int64_t hidden
  *   hidden    a positive multiple of 4.
  *   out_q     device e4m3 codes, row-major with row length `hidden`; it may have more rows
  *             than num_tokens (a padded output): rows past num_tokens are not touched.
- *             8-byte aligned (4-byte when 16-bit rows have hidden % 8 != 0).
+ *             8-byte aligned for 16-bit input with hidden % 8 == 0, else 4-byte.
  *   out_s     device float scales, one per row; entries past num_tokens are not touched.
  * Returns PTGQ_OK or a negative status (checked before launching).
  */
