@@ -389,6 +389,15 @@ def workloads():
         "masked_silu": Workload("masked_silu", "masked EP-MoE bf16 [32,384,2x4096], masked_m "
                                 "uniform in [0,384], fused silu, G=128, e4m3, UE8M0 packed "
                                 "column-major", synth.masked_silu, silu=True, fmt=1, layout=1),
+        "silu_flat_fp16": Workload("silu_flat_fp16", "fused silu*up, fp16 [8192, 2x2048] -> "
+                                   "e4m3 [8192,2048], G=128, fp32 column-major scales",
+                                   lambda: synth.silu_flat(dtype=torch.float16), silu=True,
+                                   layout=1),
+        "masked_silu_fp16": Workload("masked_silu_fp16", "masked EP-MoE fp16 [32,384,2x4096], "
+                                     "masked_m uniform in [0,384], fused silu, G=128, e4m3, "
+                                     "UE8M0 packed column-major",
+                                     lambda: synth.masked_silu(dtype=torch.float16), silu=True,
+                                     fmt=1, layout=1),
         "masked_decode": Workload("masked_decode", "masked EP-MoE decode: bf16 [32,384,2x4096] "
                                   "buffer, 1 live row per expert (masked_m = 1), fused silu, "
                                   "G=128, e4m3, UE8M0 packed column-major, no expected_m hint",
@@ -732,8 +741,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat_outliers",
                     choices=["flat_outliers", "flat_small", "silu_flat", "masked_silu",
-                             "masked_decode", "masked_decode_hint", "sweep_big", "per_token",
-                             "requant"], help="workload of the JSON line (default: the "
+                             "silu_flat_fp16", "masked_silu_fp16", "masked_decode",
+                             "masked_decode_hint", "sweep_big", "per_token", "requant"], help="workload of the JSON line (default: the "
                     "benchmarked flat_outliers)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")

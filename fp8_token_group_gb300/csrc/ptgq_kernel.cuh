@@ -56,8 +56,8 @@ struct Slot {
 // the next batch's loads are issued before the current batch is computed, and the CTAs per
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
 // CTAs/SM (64 registers).  bf16 silu, 3 CTAs/SM: flat one task pipelined, masked two tasks
-// loaded then computed.  fp16 silu: pipelined at 2 CTAs/SM (its per-element exponential
-// needs the registers).  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE / _MIN_BLOCKS override all
+// loaded then computed.  fp16 silu: one task at 2 CTAs/SM, not pipelined (its per-element
+// exponential needs the registers and keeps the instance issue-bound).  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE / _MIN_BLOCKS override all
 // instances (sweeps).
 #ifndef PTGQ_TUNE_SILU_BATCH
 #define PTGQ_TUNE_SILU_BATCH 1
@@ -76,7 +76,7 @@ struct Tuning {
   static constexpr int min_blocks = PTGQ_TUNE_MIN_BLOCKS;
 #else
   static constexpr int batch = (kLight || (kSilu && (kFp16 || !kMasked))) ? 1 : 2;
-  static constexpr bool pipeline = kSilu && (kFp16 || !kMasked);
+  static constexpr bool pipeline = kSilu && !kFp16 && !kMasked;
   static constexpr int min_blocks = kLight ? 6 : (!kSilu ? 4 : (kFp16 ? 2 : 3));
 #endif
 };
