@@ -32,15 +32,14 @@
 
 namespace ptgq {
 
-constexpr int kExpIntWords = PTGQ_EXP_INT_WORDS;     // (hi, lo) pairs, padded to 16 bytes
-constexpr int kExpFracWords = PTGQ_EXP_FRAC_WORDS;
+constexpr int kSiluF16Words = 2 * 2 * 2048;          // tables A and B, (hi, lo) pairs
 constexpr int kSiluBf16Words = 2 * PTGQ_SILU_BF16_SPAN;
 
 template <bool kFp16, bool kSilu>
 struct SmemTables {
-  // bf16 silu reads the precomputed table of results; fp16 silu rebuilds exp
-  // from the (hi, lo) exp tables.
-  static constexpr int words = !kSilu ? 0 : (kFp16 ? kExpIntWords + kExpFracWords : kSiluBf16Words);
+  // bf16 silu reads the precomputed table of results; fp16 silu forms exp(-g) from the
+  // two tables of its split exponent.
+  static constexpr int words = !kSilu ? 0 : (kFp16 ? kSiluF16Words : kSiluBf16Words);
   static constexpr int bytes = (words * 4 + 15) / 16 * 16;
 };
 
@@ -56,8 +55,8 @@ struct Slot {
 // the next batch's loads are issued before the current batch is computed, and the CTAs per
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
 // CTAs/SM (64 registers).  bf16 silu, 3 CTAs/SM: flat one task pipelined, masked two tasks
-// loaded then computed.  fp16 silu: one task at 2 CTAs/SM, not pipelined (its per-element
-// exponential needs the registers and keeps the instance issue-bound).  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE / _MIN_BLOCKS override all
+// loaded then computed.  fp16 silu, 3 CTAs/SM: one task, not pipelined (its exponential
+// from two tables and its division keep the instance issue-bound).  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE / _MIN_BLOCKS override all
 // instances (sweeps).
 #ifndef PTGQ_TUNE_SILU_BATCH
 #define PTGQ_TUNE_SILU_BATCH 1
@@ -77,7 +76,7 @@ struct Tuning {
 #else
   static constexpr int batch = (kLight || (kSilu && (kFp16 || !kMasked))) ? 1 : 2;
   static constexpr bool pipeline = kSilu && !kFp16 && !kMasked;
-  static constexpr int min_blocks = kLight ? 6 : (!kSilu ? 4 : (kFp16 ? 2 : 3));
+  static constexpr int min_blocks = kLight ? 6 : (!kSilu ? 4 : 3);
 #endif
 };
 
@@ -98,8 +97,8 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
   // Module constants first (asynchronously): they do not depend on the previous grid.
   if constexpr (kSilu) {
     if constexpr (kFp16) {
-      copy_to_smem_async(smem, kExpIntHL, kExpIntWords / 4);
-      copy_to_smem_async(smem + 4 * kExpIntWords, kExpFracHL, kExpFracWords / 4);
+      copy_to_smem_async(smem, kSiluF16A, kSiluF16Words / 8);
+      copy_to_smem_async(smem + 2 * kSiluF16Words, kSiluF16B, kSiluF16Words / 8);
     } else {
       copy_to_smem_async(smem, kSiluBf16, kSiluBf16Words / 4);
     }
@@ -183,12 +182,12 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
     uint32_t amax_bits;
     if constexpr (kSilu) {
       if constexpr (kFp16) {
-        const float2* ei = reinterpret_cast<const float2*>(silu_tab);
-        const float2* ef = ei + kExpIntWords / 2;
+        const float2* ta = reinterpret_cast<const float2*>(silu_tab);
+        const float2* tb = ta + 2048;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float s0 = silu_generic(widen_lo<true>(a.w[i]), ei, ef, PTGQ_EXP_INT_MIN, PTGQ_EXP_FRAC_JMIN);
-          const float s1 = silu_generic(widen_hi<true>(a.w[i]), ei, ef, PTGQ_EXP_INT_MIN, PTGQ_EXP_FRAC_JMIN);
+          const float s0 = silu_f16(a.w[i] & 0xFFFFu, ta, tb, PTGQ_SILU_F16_OVERFLOW_BITS);
+          const float s1 = silu_f16(a.w[i] >> 16, ta, tb, PTGQ_SILU_F16_OVERFLOW_BITS);
           v[i] = mul2(pk2(s0, s1), widen2<true>(b.w[i]));
         }
       } else {

@@ -12,6 +12,9 @@
 
 #include <cstdint>
 #include <cmath>
+#ifdef __CUDACC__
+#include <cuda_fp16.h>
+#endif
 
 #ifdef __CUDACC__
 #define PTGQ_HD __host__ __device__ __forceinline__
@@ -36,82 +39,35 @@ PTGQ_HD uint32_t f2u(float f) {
 #endif
 }
 
-// ---------------------------------------------------------------------------
-// exp for 16-bit inputs.
-//
-// Returns RN(e^x) (correctly rounded binary32) for x a bf16 or fp16 value in
-// [-20, 88.72).  Below -20 it returns 0 and from 88.72 it returns +inf; the
-// caller only feeds the result into D = RN(1 + E), which is 1 for every E below
-// 2^-24 (x < -16.6) and +inf for every E that overflows, so those limits do not
-// change D.
-//
-// Method (Tang-style table reduction, evaluated in double-float):
-//   i = rint(x) capped at 88, f = x - i        (exact; |f| <= 0.72)
-//   j = rint(128 f),           r = f - j/128   (exact; |r| <= 1/256, <= 11 bits)
-//   e^x = e^i * e^(j/128) * (1 + r + r^2/2 + c),  c = r^3/6 + r^4/24 + r^5/120
-// e^i and e^(j/128) come from (hi, lo) tables accurate to ~2^-48; r^2 is exact
-// because r has at most 11 significant bits; products with the large terms are
-// split exactly with fma, and the last partial sum is rounded to odd, so the final
-// addition rounds a value within ~2^-45 of e^x once, on the correct side of every
-// rounding midpoint.  Checked against 100-bit values for every bf16 and fp16 input.
-// ---------------------------------------------------------------------------
-PTGQ_HD float exp_from_tables(float x, const float2* exp_int, const float2* exp_frac,
-                              int int_min, int frac_jmin) {
-  // Clamp into the tables' range; results outside [-20, 88.72) are replaced below.
-  const float xc = fminf(fmaxf(x, -20.0f), 88.75f);
-  float fi = rintf(xc);
-  fi = fminf(fi, 88.0f);
-  const float f = xc - fi;
-  const float fj = rintf(f * 128.0f);
-  const float r = fmaf(fj, -0.0078125f, f);
-  const float2 A = exp_int[static_cast<int>(fi) - int_min];
-  const float2 B = exp_frac[static_cast<int>(fj) - frac_jmin];
-  // T = A * B as an unevaluated sum th + tl
-  const float th = A.x * B.x;
-  float tl = fmaf(A.x, B.x, -th);
-  tl = fmaf(A.x, B.y, tl);
-  tl = fmaf(A.y, B.x, tl);
-  // series of e^r - 1 = r + h2 + c
-  const float h2 = 0.5f * (r * r);
-  float c = fmaf(r, 1.0f / 60.0f, 1.0f / 12.0f);
-  c = fmaf(r, c, 1.0f / 3.0f);
-  c = (h2 * r) * c;
-  // th * r and th * h2, each split exactly into a rounded part and its error
-  const float m1 = th * r;
-  const float m1l = fmaf(th, r, -m1);
-  const float m2 = th * h2;
-  const float m2l = fmaf(th, h2, -m2);
-  // th + m1 + m2 with the rounding errors of both additions kept
-  const float s1 = th + m1;
-  const float e1 = (th - s1) + m1;
-  const float s2 = s1 + m2;
-  const float e2 = (s1 - s2) + m2;
-  // Everything below e1 (each term < 2^-24 th), then e1 added with round-to-odd:
-  // the sticky last bit tells the final rounding on which side of a midpoint the
-  // value lies (x = 2^-24 is such a case: e^x = 1 + 2^-24 + 2^-49 + ...).
-  float rest = fmaf(th, c, tl);
-  rest = fmaf(tl, r, rest);
-  rest = rest + (m1l + m2l);
-  const float inner = e2 + rest;
-  const float w = e1 + inner;
-  const float wz = w - e1;
-  const float werr = (e1 - (w - wz)) + (inner - wz);
-  uint32_t wb = f2u(w);
-  if (werr != 0.0f && (wb & 1u) == 0u) wb += ((werr > 0.0f) == (w > 0.0f)) ? 1u : 0xFFFFFFFFu;
-  float res = s2 + u2f(wb);
-  res = x < -20.0f ? 0.0f : res;
-  res = x >= 88.72f ? INFINITY : res;
-  return res;
-}
-
-// silu(g) = g / (1 + exp(-g)) with the binary32 step sequence E, D = RN(1 + E),
-// S = RN(g / D) (sglang PR #30924, "Implementation breakdown" item 1: the fused
-// silu_and_mul trait).
-PTGQ_HD float silu_generic(float g, const float2* exp_int, const float2* exp_frac, int int_min,
-                           int frac_jmin) {
-  const float e = exp_from_tables(-g, exp_int, exp_frac, int_min, frac_jmin);
-  const float d = 1.0f + e;
-  return g / d;
+// silu(g) = g / (1 + exp(-g)) with the binary32 step sequence E = RN(exp(-g)),
+// D = RN(1 + E), S = RN(g / D) (sglang PR #30924, "Implementation breakdown" item 1: the
+// fused silu_and_mul trait), for an fp16 gate g given by its bits h.  With x = -g,
+// exp(x) = exp(x_hi) * exp(x_lo): x_hi keeps the sign, exponent and top five mantissa bits
+// of x, x_lo the rest.  Table A holds exp(x_hi) at [bits(x) >> 5], table B exp(x_lo) at
+// [sign][exponent][low five bits], each as a (hi, lo) binary32 pair.  E is their product
+// in double-float, rounded once; S = RN(g / D) from the correctly rounded reciprocal r and
+// one fma correction (q0 = RN(g r), q = RN(q0 + (g - q0 D) r)).  The generator of the
+// tables replays these operations in exact arithmetic for every fp16 gate: the result is
+// S exactly, except for two closed forms, g <= -88.75 (exp(-g) overflows binary32, so
+// S = -0) and g = -0 (S = -0).
+__device__ __forceinline__ float silu_f16(uint32_t h, const float2* ta, const float2* tb,
+                                          uint32_t overflow_bits) {
+  const float g = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+  const uint32_t hx = h ^ 0x8000u;                                     // bits of x = -g
+  const float2 a = ta[hx >> 5];
+  const float2 b = tb[((hx >> 5) & 0x7E0u) | (hx & 0x1Fu)];
+  const float p = __fmul_rn(a.x, b.x);
+  float t = __fmaf_rn(a.x, b.x, -p);
+  t = __fmaf_rn(a.y, b.x, t);
+  t = __fmaf_rn(a.x, b.y, t);
+  const float d = __fadd_rn(1.0f, __fadd_rn(p, t));
+  const float r = __frcp_rn(d);
+  const float q0 = __fmul_rn(g, r);
+  const float res = __fmaf_rn(-q0, d, g);
+  float s = __fmaf_rn(res, r, q0);
+  s = (h & 0x7FFFu) == 0u ? g : s;
+  s = (hx < 0x8000u && hx >= overflow_bits) ? -0.0f : s;
+  return s;
 }
 
 // The same sequence for a bf16 gate, read from the precomputed table of binary32
