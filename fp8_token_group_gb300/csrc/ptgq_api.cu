@@ -250,13 +250,14 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   cfg.attrs = attr;
   cfg.numAttrs = (flags & PTGQ_FLAG_NO_PDL) ? 0 : 1;
   void* args[] = {&p};
-  // A failed launch is reported through the status code; the runtime's error state is
-  // cleared so it does not surface later in the caller's own CUDA calls.
+  // A failed launch is reported through the status code and its error is cleared from the
+  // runtime's state, so it does not surface later in the caller's own CUDA calls.  After a
+  // successful launch the error state is left alone: an error pending from the caller's
+  // earlier work is theirs to see, not this call's to report or clear.
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
     cudaGetLastError();
     return PTGQ_ERR_CUDA;
   }
-  if (cudaGetLastError() != cudaSuccess) return PTGQ_ERR_CUDA;
   return PTGQ_OK;
 }
 

@@ -361,13 +361,14 @@ int launch(const void* fn, int grid, size_t smem, ptgq_stream_t stream, void** a
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // A failed launch is reported through the status code; the runtime's error state is
-  // cleared so it does not surface later in the caller's own CUDA calls.
+  // A failed launch is reported through the status code and its error is cleared from the
+  // runtime's state, so it does not surface later in the caller's own CUDA calls.  After a
+  // successful launch the error state is left alone: an error pending from the caller's
+  // earlier work is theirs to see, not this call's to report or clear.
   if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
     cudaGetLastError();
     return PTGQ_ERR_CUDA;
   }
-  if (cudaGetLastError() != cudaSuccess) return PTGQ_ERR_CUDA;
   return PTGQ_OK;
 }
 

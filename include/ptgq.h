@@ -29,7 +29,8 @@
  *     one kernel per call on `stream`, so a call can be captured in a CUDA graph.
  *   - Errors are returned as negative status codes (below) before anything is
  *     launched; nothing is written in that case.  No exception crosses the ABI.
- *     PTGQ_ERR_CUDA reports a launch failure taken from cudaGetLastError().
+ *     PTGQ_ERR_CUDA reports a failed launch (the launch call's own status; that error
+ *     is then cleared from the CUDA runtime's state).
  *   - The kernel is launched with programmatic stream serialization (PDL): it may
  *     start while the previous kernel on `stream` finishes, and waits for it
  *     (griddepcontrol.wait) before touching memory.
