@@ -15,6 +15,7 @@ Typical use::
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import re
 import threading
@@ -91,14 +92,22 @@ def strerror(status: int) -> str:
     return lib().ptgq_strerror(status).decode()
 
 
+@functools.lru_cache(maxsize=1024)
 def scale_elems(n: int, tokens_pad: int, hidden: int, group_size: int, scale_fmt: int,
                 scale_layout: int, masked: bool) -> int:
+    """Scale elements (floats, or int32 words when packed) out_s must hold; see
+    ``ptgq_scale_elems``."""
     out = ctypes.c_int64(0)
     rc = lib().ptgq_scale_elems(n, tokens_pad, hidden, group_size, scale_fmt, scale_layout,
                                 int(bool(masked)), ctypes.byref(out))
     if rc != 0:
         raise PtgqError(rc, "ptgq_scale_elems")
     return out.value
+
+
+def hidden_ok(hidden: int, group_size: int) -> bool:
+    """Whether the size query is meaningful (otherwise the library rejects the call itself)."""
+    return group_size in (16, 32, 64, 128) and hidden > 0 and hidden % group_size == 0
 
 
 def _in_dtype(t):
@@ -161,6 +170,21 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
     else:
         n, hin = x.shape
     H = hin // 2 if fuse_silu else hin
+    # The library sees raw pointers; check here that the outputs hold what the call writes,
+    # so a short buffer is an exception rather than a write past its end.
+    rows = tokens_pad if masked_m is not None else (tokens_pad or n)
+    need_q = (n if masked_m is not None else 1) * rows * H
+    if out_q.numel() * out_q.element_size() < need_q:
+        raise ValueError(f"out_q holds {out_q.numel() * out_q.element_size()} bytes; "
+                         f"the call writes up to {need_q}")
+    if hidden_ok(H, group_size):
+        need_s = 4 * scale_elems(n, tokens_pad, H, group_size, scale_fmt, scale_layout,
+                                 masked_m is not None)
+        if out_s.numel() * out_s.element_size() < need_s:
+            raise ValueError(f"out_s holds {out_s.numel() * out_s.element_size()} bytes; "
+                             f"the call writes up to {need_s}")
+    if masked_m is not None and masked_m.numel() < n:
+        raise ValueError(f"masked_m has {masked_m.numel()} entries for {n} experts")
     handle = _stream_handle(stream, x.get_device() if x.is_cuda else None)
     rc = (_lib or lib()).ptgq_quant_ex(
         x.data_ptr(), _in_dtype(x), n, tokens_pad, H, group_size, out_q.data_ptr(), out_dtype,
@@ -220,6 +244,10 @@ def per_token_quant(x, out_q, out_s, *, num_tokens: int | None = None, stream=No
         raise TypeError(f"unsupported dtype {x.dtype}")
     T, hidden = x.shape
     n = T if num_tokens is None else num_tokens
+    if not 0 <= n <= T:
+        raise ValueError(f"num_tokens {n} outside [0, {T}]")
+    if out_q.numel() * out_q.element_size() < n * hidden or out_s.numel() < n:
+        raise ValueError("out_q must hold num_tokens * hidden codes and out_s num_tokens scales")
     rc = lib().ptgq_per_token_quant(x.data_ptr(), dt, n, hidden, out_q.data_ptr(),
                                     out_s.data_ptr(), _stream_handle(stream, x.device))
     if rc != 0:
@@ -236,6 +264,17 @@ def requant_per_tensor(x, x_scale, masked_m, output_scale, out, *, group_size: i
         raise ValueError("x and out must be contiguous CUDA tensors")
     E, M, K = x.shape
     se, sm, sg = x_scale.stride()
+    if out.numel() * out.element_size() < E * M * K:
+        raise ValueError("out must hold E * M * K codes")
+    if E * M > 0 and group_size in (16, 32, 64, 128) and K % group_size == 0:
+        reach = (E - 1) * se + (M - 1) * sm + (K // group_size - 1) * sg + 1
+        avail = x_scale.untyped_storage().nbytes() // 4 - x_scale.storage_offset()
+        if min(se, sm, sg) < 0 or reach > avail:
+            raise ValueError("x_scale's strides reach past its storage")
+    if masked_m is not None and masked_m.numel() < E:
+        raise ValueError(f"masked_m has {masked_m.numel()} entries for {E} experts")
+    if output_scale.numel() < 1:
+        raise ValueError("output_scale must hold one float")
     rc = lib().ptgq_requant_per_tensor(
         x.data_ptr(), x_scale.data_ptr(), se, sm, sg,
         None if masked_m is None or E == 0 else masked_m.data_ptr(), output_scale.data_ptr(),

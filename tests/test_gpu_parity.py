@@ -348,6 +348,49 @@ def test_device_arguments_rejected_before_launch():
     assert rc == -6
 
 
+def test_binding_rejects_short_buffers_before_launch():
+    """The library sees raw pointers; the binding checks that the outputs hold what a call
+    writes, so a short buffer raises instead of being written past its end.  Nothing is
+    launched: the sentinel contents stay."""
+    x = synth.flat_small()
+    xd = x.cuda()
+    kw = dict(scale_fmt=P.SCALE_UE8M0_PACKED, scale_layout=P.COL_MAJOR_TMA)
+    q, s = P.alloc_outputs(xd, 128, **kw)
+    q.view(torch.uint8).fill_(0x7F)
+    s.fill_(-1)
+    with pytest.raises(ValueError, match="out_s"):
+        P.quant(xd, q, s[:-1], 128, **kw)
+    with pytest.raises(ValueError, match="out_q"):
+        P.quant(xd, q[:-1], s, 128, **kw)
+    with pytest.raises(ValueError, match="out_q"):
+        P.quant(xd, q, s, 128, tokens_pad=80, **kw)           # padding rows need more room
+    xm, mm = synth.masked_silu(experts=4, tokens_pad=32, hidden=256)
+    xmd, mmd = xm.cuda(), mm.cuda()
+    qm, sm = P.alloc_outputs(xmd, 128, fuse_silu=True, masked=True, **kw)
+    with pytest.raises(ValueError, match="masked_m"):
+        P.quant(xmd, qm, sm, 128, fuse_silu=True, masked_m=mmd[:3], **kw)
+    with pytest.raises(ValueError, match="out_s"):
+        P.quant(xmd, qm, sm[:-1], 128, fuse_silu=True, masked_m=mmd, **kw)
+    xt = torch.randn(16, 512, device="cuda").to(torch.bfloat16)
+    qt = torch.empty((16, 512), dtype=torch.float8_e4m3fn, device="cuda")
+    st = torch.empty(16, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError, match="out_q"):
+        P.per_token_quant(xt, qt, st[:15])
+    with pytest.raises(ValueError, match="num_tokens"):
+        P.per_token_quant(xt, qt, st, num_tokens=17)
+    codes = torch.zeros((2, 8, 256), dtype=torch.uint8, device="cuda")
+    xs = torch.ones((2, 8, 2), dtype=torch.float32, device="cuda")
+    osc = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError, match="out must hold"):
+        P.requant_per_tensor(codes, xs, None, osc,
+                             torch.empty(2 * 7 * 256, dtype=torch.uint8, device="cuda"))
+    with pytest.raises(ValueError, match="x_scale"):         # one group's scales, two groups
+        P.requant_per_tensor(codes, torch.ones((2, 8, 1), device="cuda"), None, osc,
+                             torch.empty_like(codes))
+    torch.cuda.synchronize()
+    assert bool((q.view(torch.uint8) == 0x7F).all()) and bool((s == -1).all())
+
+
 def test_masked_4096_experts_mostly_empty():
     """The largest expert count, with many empty and one-row experts: exercises the
     row-to-expert buckets across runs of empty experts."""
