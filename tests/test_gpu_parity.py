@@ -348,6 +348,45 @@ def test_device_arguments_rejected_before_launch():
     assert rc == -6
 
 
+def test_concurrent_calls_from_threads_on_their_own_streams():
+    """Eight host threads, each on its own stream and with its own variant (scale format,
+    layout, output type, silu), call the library repeatedly at once: the launcher's shared
+    occupancy and attribute caches are hit concurrently, and every result still matches
+    the oracle bit for bit."""
+    import threading
+    cases = [Case(scale_fmt=FMTS[i % 3], layout=LAYOUTS[i % 2], out_dtype=(P.E4M3, P.INT8)[(i // 2) % 2],
+                  silu=bool(i & 4), group=(128, 64, 32, 16)[i % 4]) for i in range(8)]
+    xs = [synth.normal((96 + 8 * i, 2048 if c.silu else 1024), torch.bfloat16, seed=50 + i)
+          for i, c in enumerate(cases)]
+    results, errors = [None] * len(cases), []
+
+    def work(i):
+        try:
+            c, xd = cases[i], xs[i].cuda()
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                q, s = P.alloc_outputs(xd, c.group, out_dtype=c.out_dtype, scale_fmt=c.scale_fmt,
+                                       scale_layout=c.layout, fuse_silu=c.silu)
+                for _ in range(25):
+                    P.quant(xd, q, s, c.group, out_dtype=c.out_dtype, scale_fmt=c.scale_fmt,
+                            scale_layout=c.layout, fuse_silu=c.silu)
+            stream.synchronize()
+            results[i] = (q.view(torch.uint8).cpu().numpy().ravel(),
+                          s.view(torch.int32).cpu().numpy().view(np.uint32).ravel())
+        except Exception as exc:           # reported below, on the main thread
+            errors.append(exc)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(cases))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for i, c in enumerate(cases):
+        oq, os_ = run_oracle(xs[i], c)
+        assert_same(results[i][0], results[i][1], oq, os_, f"thread {i} {c}")
+
+
 def test_binding_rejects_short_buffers_before_launch():
     """The library sees raw pointers; the binding checks that the outputs hold what a call
     writes, so a short buffer raises instead of being written past its end.  Nothing is
