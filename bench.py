@@ -384,7 +384,7 @@ def workloads():
         "flat_small": Workload("flat_small", "flat bf16 x[64,4096] N(0,1), G=128, e4m3, fp32 "
                                "row-major scales [64,32]", synth.flat_small),
         "silu_flat": Workload("silu_flat", "fused silu*up, bf16 [8192, 2x2048] -> e4m3 "
-                              "[8192,2048], G=128, fp32 column-major scales [32,8192]",
+                              "[8192,2048], G=128, fp32 column-major scales [16,8192]",
                               synth.silu_flat, silu=True, layout=1),
         "masked_silu": Workload("masked_silu", "masked EP-MoE bf16 [32,384,2x4096], masked_m "
                                 "uniform in [0,384], fused silu, G=128, e4m3, UE8M0 packed "
