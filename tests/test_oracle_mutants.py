@@ -11,6 +11,7 @@ import pytest
 
 import oracle as O
 import test_oracle_pins as pins
+import test_oracle_pins_bounds as bpins
 
 SRC = os.path.join(os.path.dirname(O.__file__), "ptgq_oracle.cpp")
 
@@ -35,6 +36,11 @@ MUTANTS = [
     ("fp16 exponent bias", "e - 25", "e - 24"),
     ("UE8M0 float off by one", "return bits_to_float(static_cast<uint32_t>(e) << 23);",
      "return bits_to_float(static_cast<uint32_t>(e + 1) << 23);"),
+    ("quotient bound half as wide", "std::ldexp(1.0, ex - 23)", "std::ldexp(1.0, ex - 24)"),
+    ("quotient bound twice as wide", "std::ldexp(1.0, ex - 23)", "std::ldexp(1.0, ex - 22)"),
+    ("quotient bound ignores the sign of k", "const double b = e + k * u;",
+     "const double b = e + (k > 0 ? k : -k) * u;"),
+    ("quotient bound ulp of the scale's binade", "std::ilogb(e)", "std::ilogb(s)"),
 ]
 
 # Fast pins: each a callable that raises when the oracle is wrong.
@@ -54,6 +60,9 @@ FAST_PINS = [
     lambda: pins.test_scale_layouts_index_and_padding(O.LAYOUT_COL, O.FMT_FP32),
     lambda: pins.test_scale_layouts_index_and_padding(O.LAYOUT_ROW, O.FMT_UE8M0_FP32),
     pins.test_masked_rows_match_flat_and_padding_untouched,
+    bpins.test_hand_ties_widen_to_both_neighbours,
+    lambda: bpins.test_bounds_part_where_a_boundary_is_within_k_ulps(bpins.silu_values_data(), O.OUT_E4M3),
+    lambda: bpins.test_bounds_part_where_a_boundary_is_within_k_ulps(bpins.silu_values_data(), O.OUT_INT8),
 ]
 
 

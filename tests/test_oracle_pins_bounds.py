@@ -116,3 +116,73 @@ def test_bounds_bracket_the_exact_codes_with_general_scales():
             val = lambda c: c.view(np.int8).astype(np.float32)
         assert np.all(val(lo) <= val(ex)) and np.all(val(ex) <= val(hi))
         assert 0 < (lo != hi).mean() < (1e-2 if out == O.OUT_E4M3 else 4e-3)
+
+
+def _e4m3_midpoints() -> np.ndarray:
+    """The rounding boundaries of the e4m3 encoder: midpoints between neighbouring finite
+    values of the format (from its value table), both signs."""
+    vals = set()
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            continue
+        v = m / 512 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        vals.add(-v if s else v)
+    vals = np.array(sorted(vals))
+    return (vals[1:] + vals[:-1]) / 2
+
+
+def silu_values_data():
+    """4M fused-silu values, from the oracle as loaded: continuous binary32 quotients,
+    unlike the 16-bit inputs, whose quotients lie either within about one ulp of a rounding
+    boundary or far from it."""
+    T, H = 2048, 2048
+    x = synth.normal((T, 2 * H), torch.bfloat16, seed=5)
+    xf = x.float().numpy()
+    f = O.lib().oracle_silu_mul
+    g, u = xf[:, :H].ravel().tolist(), xf[:, H:].ravel().tolist()
+    v = np.fromiter((f(a, b) for a, b in zip(g, u)), dtype=np.float64, count=len(g))
+    return x, v, T, H
+
+
+@pytest.fixture(scope="module")
+def silu_values():
+    return silu_values_data()
+
+
+@pytest.mark.parametrize("out", [O.OUT_E4M3, O.OUT_INT8])
+def test_bounds_part_where_a_boundary_is_within_k_ulps(silu_values, out):
+    """Independent of the oracle's bound arithmetic: with the exact quotient y = v / s (in
+    binary64, far finer than a binary32 ulp) and the encoder's rounding boundaries (e4m3
+    midpoints from the format's value table, or half-integers for int8), the k = 2 bounds
+    must part wherever a boundary lies within 1.95 ulps of y and never where it lies beyond
+    3.05 ulps (the bound is rounded outward, which can add up to one ulp).  Enough quotients
+    fall in both bands that a bound of half or twice the width fails here."""
+    x, v, T, H = silu_values
+    bits = synth.bits_u16(x)
+
+    def run(k):
+        q = np.zeros(T * H, np.uint8)
+        s = np.zeros(T * (H // 128), np.float32)
+        O.quant(bits, O.IN_BF16, T, 0, H, 128, q, out, s, O.FMT_FP32, O.LAYOUT_ROW, 1, None,
+                1e-10, 0, k)
+        return q, s
+
+    lo, s = run(-2)
+    hi, _ = run(2)
+    y = v / np.repeat(s.astype(np.float64), 128)
+    ulp = np.spacing(np.abs(y).astype(np.float32)).astype(np.float64)
+    if out == O.OUT_E4M3:
+        mids = _e4m3_midpoints()
+        j = np.searchsorted(mids, y)
+        d = np.minimum(np.abs(y - mids[np.clip(j - 1, 0, len(mids) - 1)]),
+                       np.abs(y - mids[np.clip(j, 0, len(mids) - 1)]))
+    else:
+        d = np.abs(y - (np.floor(y) + 0.5))
+        d[np.abs(y) > 127.4] = np.inf           # saturated: no boundary to cross
+    r = d / ulp
+    parted = lo != hi
+    near, far = r < 1.95, r > 3.05
+    assert ((r > 1) & near).sum() >= 3 and (far & (r < 5)).sum() >= 10
+    assert np.all(parted[near]), int((near & ~parted).sum())
+    assert not np.any(parted[far]), int((far & parted).sum())
