@@ -8,14 +8,17 @@ import subprocess
 import tempfile
 
 import pytest
+import torch
 
 import oracle as O
 import test_oracle_pins as pins
 import test_oracle_pins_bounds as bpins
+import test_oracle_pins_next as npins
 
 SRC = os.path.join(os.path.dirname(O.__file__), "ptgq_oracle.cpp")
 
-# (name, original text, mutated text)
+# (name, original text, mutated text).  Every mutant keeps the oracle's memory accesses in
+# bounds: the mutated library runs inside the test process.
 MUTANTS = [
     ("amax without abs", "amax = std::fmax(amax, std::fabs(v[i]));", "amax = std::fmax(amax, v[i]);"),
     ("no eps floor", "amax = std::fmax(amax, eps);", ""),
@@ -41,19 +44,31 @@ MUTANTS = [
     ("quotient bound ignores the sign of k", "const double b = e + k * u;",
      "const double b = e + (k > 0 ? k : -k) * u;"),
     ("quotient bound ulp of the scale's binade", "std::ilogb(e)", "std::ilogb(s)"),
+    # per-token (whole-row) quantization
+    ("per-token divides instead of multiplying by the reciprocal", "float y = val(i) * inv;",
+     "float y = s == 0.0f ? 0.0f : val(i) / s;"),
+    ("per-token zero row unguarded", "const float inv = s == 0.0f ? 0.0f : 1.0f / s;",
+     "const float inv = 1.0f / s;"),
+    ("per-token max without abs", "m = std::fmax(m, std::fabs(val(i)));", "m = std::fmax(m, val(i));"),
+    ("per-token scale with the wrong FMAX", "const float s = m / 448.0f;", "const float s = m / 480.0f;"),
+    # per-token-group -> per-tensor requantization
+    ("requant multiplies by the output scale", "const float inv = 1.0f / output_scale;",
+     "const float inv = output_scale;"),
+    ("requant product order", "const float y = (e4m3_decode(x[i]) * sc) * inv;",
+     "const float y = e4m3_decode(x[i]) * (sc * inv);"),
+    ("requant ignores masked_m", "int64_t live = masked_m[e];", "int64_t live = M;"),
+    ("requant group index from the row", "(k / group_size) * stride_g", "(m / group_size) * stride_g"),
 ]
 
 # Fast pins: each a callable that raises when the oracle is wrong.
 FAST_PINS = [
     pins.test_e4m3_hand_ties_fixture,
     pins.test_int8_encoder_vs_numpy_rint_clip,
-    pins.test_e4m3_encoder_vs_exhaustive_argmin_and_saturation,
     pins.test_ue8m0_closed_forms,
     pins.test_silu_mul_closed_forms_and_error_bound,
     lambda: pins.test_fp16_decode_matches_numpy_all_patterns(),
     lambda: pins.test_vllm_all_zero_worked_example(5),
     pins.test_all_zero_without_floor_closed_form,
-    pins.test_integer_rows_exact_closed_form,
     pins.test_mantissa_rounds_up,
     lambda: pins.test_random_rows_vs_library_composition(128, O.OUT_E4M3, O.FMT_FP32),
     lambda: pins.test_scale_layouts_index_and_padding(O.LAYOUT_COL, O.FMT_UE8M0_PACKED),
@@ -61,9 +76,25 @@ FAST_PINS = [
     lambda: pins.test_scale_layouts_index_and_padding(O.LAYOUT_ROW, O.FMT_UE8M0_FP32),
     pins.test_masked_rows_match_flat_and_padding_untouched,
     bpins.test_hand_ties_widen_to_both_neighbours,
-    lambda: bpins.test_bounds_part_where_a_boundary_is_within_k_ulps(bpins.silu_values_data(), O.OUT_E4M3),
-    lambda: bpins.test_bounds_part_where_a_boundary_is_within_k_ulps(bpins.silu_values_data(), O.OUT_INT8),
+    lambda: npins.test_per_token_vs_library_composition(torch.bfloat16, 1076),
+    lambda: npins.test_per_token_vs_library_composition(torch.float32, 1368),
+    npins.test_per_token_integer_rows_exact,
+    npins.test_per_token_midpoint_rounding_and_padded_tail,
+    lambda: npins.test_requant_masked_rows_and_k_tail(1152),
+    npins.test_requant_vs_library_composition_and_saturation,
+    npins.test_per_token_multiplies_by_the_reciprocal,
+    npins.test_requant_scales_first_then_the_output_scale,
+    # the slow ones last (several seconds each), so most mutants fail before reaching them
+    pins.test_e4m3_encoder_vs_exhaustive_argmin_and_saturation,
+    pins.test_integer_rows_exact_closed_form,
+    lambda: _bound_width_pins(),                       # 4M silu values
 ]
+
+
+def _bound_width_pins():
+    data = bpins.silu_values_data()
+    for out in (O.OUT_E4M3, O.OUT_INT8):
+        bpins.test_bounds_part_where_a_boundary_is_within_k_ulps(data, out)
 
 
 def _build_mutant(src_text: str, tmp: str) -> str:

@@ -132,3 +132,75 @@ def test_requant_vs_library_composition_and_saturation():
     assert np.array_equal(out[0], ref[0]) and np.array_equal(out[2], ref[2])
     assert np.array_equal(out[1, :7], ref[1, :7]) and np.all(out[1, 7:] == 0)
     assert (np.abs(y) > 448).any()                        # saturation was exercised
+
+
+# ---------------------------------------------------------------- operation order
+
+def _bits_plus(a: np.ndarray, d: int) -> np.ndarray:
+    return (np.asarray(a, np.float32).view(np.int32) + np.int32(d)).view(np.float32)
+
+
+def test_per_token_multiplies_by_the_reciprocal():
+    """The page's per-token kernel multiplies by inv = RN(1/s); a division by s gives other
+    codes for some inputs.  Rows are built (seeded search, binary32 numpy arithmetic) from
+    values within a few ulps of e4m3 midpoints times s, kept where the two orders part;
+    the oracle must follow the reciprocal order on every one of them."""
+    rng = np.random.default_rng(7)
+    ties = np.array([1.0625, 1.1875, 2.125, 17.0, 19.0, 0.0029296875, 104.0, 208.0, 3.25, 6.5])
+    rows = []
+    while len(rows) < 8:
+        m = F32(rng.uniform(1, 1000))
+        s = F32(m / F32(448))
+        inv = F32(F32(1) / s)
+        cand = np.concatenate([_bits_plus((ties * np.float64(s)).astype(np.float32), d)
+                               for d in (-2, -1, 0, 1, 2)])
+        a = e4m3_bytes(np.clip(cand * inv, -448, 448))
+        b = e4m3_bytes(np.clip(cand / s, -448, 448))
+        keep = cand[a != b]
+        if keep.size:
+            rows.append(np.concatenate([[m], keep[:7], np.zeros(7 - min(7, keep.size), np.float32)]))
+    x = torch.from_numpy(np.stack(rows).astype(np.float32))
+    q, s = _pt(x)
+    rq, rs = _pt_reference(x)                       # x * RN(1/s), numpy binary32
+    assert np.array_equal(q, rq) and np.array_equal(s.view(np.uint32), rs.view(np.uint32))
+    v = x.numpy()
+    by_division = e4m3_bytes(np.clip(v / rs[:, None], -448, 448)).reshape(v.shape)
+    assert (by_division != q).sum() >= 8             # the rows do tell the two orders apart
+
+
+def test_requant_scales_first_then_the_output_scale():
+    """The page's requant forms (v * x_scale) * (1 / output_scale); the other association,
+    v * (x_scale * (1 / output_scale)), gives other codes for some inputs.  Groups are built
+    by a seeded search aiming v * x_scale / output_scale at e4m3 midpoints, kept where the
+    two orders part; the oracle must follow the page's order."""
+    rng = np.random.default_rng(11)
+    vals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    mags = np.unique(np.abs(vals[np.isfinite(vals)]))
+    mids = (mags[1:] + mags[:-1]) / 2
+    nz = [c for c in range(1, 127) if np.isfinite(vals[c]) and vals[c] != 0]
+    os_ = F32(2.243415355682373)
+    inv = F32(F32(1) / os_)
+    picks = []
+    while len(picks) < 8:
+        c = int(rng.choice(nz))
+        sc0 = F32(float(rng.choice(mids)) * float(os_) / float(vals[c]))
+        for d in range(-3, 4):
+            sc = _bits_plus(np.array([sc0]), d)
+            a = e4m3_bytes(np.clip((vals[c] * sc).astype(np.float32) * inv, -448, 448))
+            b = e4m3_bytes(np.clip(vals[c] * (sc * inv).astype(np.float32), -448, 448))
+            if a[0] != b[0]:
+                picks.append((c, float(sc[0])))
+                break
+    G, M = 128, len(picks)
+    codes = np.zeros((1, M, G), np.uint8)
+    xs = np.zeros((1, M, 1), np.float32)
+    for r, (c, sc) in enumerate(picks):
+        codes[0, r, :] = c
+        xs[0, r, 0] = sc
+    out = np.zeros_like(codes)
+    O.requant_per_tensor(codes, xs, (M, 1, 1), np.array([M], np.int32), float(os_), out)
+    v = vals[codes.astype(np.int64)]
+    page = e4m3_bytes(np.clip((v * xs).astype(np.float32) * inv, -448, 448)).reshape(codes.shape)
+    other = e4m3_bytes(np.clip(v * (xs * inv).astype(np.float32), -448, 448)).reshape(codes.shape)
+    assert np.array_equal(out, page)
+    assert (other != out).sum() >= 8 * G
