@@ -29,6 +29,8 @@ MUTANTS = [
     ("no saturation", "if (a > 448.0) a = 448.0;", ""),
     ("silu exp sign", "const float e = exp_f32(-g);", "const float e = exp_f32(g);"),
     ("silu 1 - e", "const float d = 1.0f + e;", "const float d = 1.0f - e;"),
+    ("silu association (g * u) / d", "  const float s = g / d;\n  return s * u;",
+     "  const float s = g * u;\n  return s / d;"),
     ("reciprocal multiply", "const float y = v[i] / scale;", "const float y = v[i] * (1.0f / scale);"),
     ("col-major transposed", "col * g.mn_pad + row", "row * g.mn_pad + col"),
     ("packed byte order", "<< (8 * j)", "<< (8 * (3 - j))"),
@@ -85,6 +87,7 @@ FAST_PINS = [
     npins.test_per_token_multiplies_by_the_reciprocal,
     npins.test_requant_scales_first_then_the_output_scale,
     # the slow ones last (several seconds each), so most mutants fail before reaching them
+    lambda: pins.test_silu_mul_every_16bit_gate("bf16"),
     pins.test_e4m3_encoder_vs_exhaustive_argmin_and_saturation,
     pins.test_integer_rows_exact_closed_form,
     lambda: _bound_width_pins(),                       # 4M silu values
