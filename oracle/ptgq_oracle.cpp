@@ -24,9 +24,18 @@
 // order written here.  Build with -ffp-contract=off and without fast-math so the
 // compiler neither fuses a multiply into an add nor reassociates.
 //
-// Parity pins: every function below is checked in tests/test_oracle_pins.py against
+// One addition is not from the pages: oracle_quant_quotient_bound gives, per element,
+// the codes of the quotient moved k binary32 ulps down or up.  It checks the library's
+// fast-math compatibility mode, whose division is only known to lie within 2 ulps of
+// the exact quotient ([sglang#34257] "Implementation notes" and [sglang#30924] "Risks"
+// report that such a division changes codes).
+//
+// Parity pins: every function below is checked in tests/test_oracle_pins.py,
+// tests/test_oracle_pins_next.py and tests/test_oracle_pins_bounds.py against
 // something other than itself (closed forms, library routines, the worked example
-// of [vllm#41326], exhaustive enumeration).  No function here is "parity unpinned".
+// of [vllm#41326], exhaustive enumeration, exact rational arithmetic), and
+// tests/test_oracle_mutants.py checks that planted mistakes fail those pins.  No
+// function here is "parity unpinned".
 
 #include <cmath>
 #include <cstdint>
