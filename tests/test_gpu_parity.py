@@ -125,6 +125,16 @@ def test_masked_expected_m_hint_changes_nothing(expected_m):
                     expected_m=expected_m), masked_m=mm.numpy())
 
 
+@pytest.mark.parametrize("fmt", [P.SCALE_UE8M0_PACKED, P.SCALE_FP32])
+def test_masked_large_pad_per_expert(fmt):
+    """A prefill-sized masked layout: 8 experts of 4096 rows, live counts up to the pad
+    (one expert full, one empty), so the row-to-expert buckets use a large shift."""
+    x = synth.normal((8, 4096, 2 * 2048), torch.bfloat16, seed=21)
+    mm = synth.masked_counts(8, 4096, seed=21).numpy()
+    mm[2], mm[5] = 4096, 0
+    compare(x, Case(silu=True, scale_fmt=fmt, layout=P.COL_MAJOR_TMA), masked_m=mm)
+
+
 def test_masked_decode_one_row_per_expert():
     """Decode-sized masked batch: one live row in each of 32 experts of 384, with and
     without the matching hint (most CTAs of the hint-less grid find no work and return)."""
