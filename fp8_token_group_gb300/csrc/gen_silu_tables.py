@@ -6,16 +6,12 @@ rounded binary32 exponential.  Gates are bf16 or fp16 values, so the exponential
 ever sees 16-bit inputs; these tables make it exact without a per-element
 double-precision evaluation:
 
-* ``kSiluF16A`` / ``kSiluF16B``  for fp16 gates: with x = -g, exp(x) = exp(x_hi) * exp(x_lo),
-  where x_hi keeps the sign, the exponent and the top five mantissa bits of the fp16 x and
-  x_lo is the rest (exact).  A holds exp(x_hi) indexed by the top 11 bits of x, B holds
-  exp(x_lo) indexed by (sign, exponent, low five mantissa bits), 2048 entries each, every
-  value as a pair of binary32 words (hi = RN(v), lo = RN(v - hi)).  The kernel forms
-  E = RN(A * B) in double-float (one exact product split by fma), D = RN(1 + E) and
-  S = RN(g / D) by the correctly rounded reciprocal plus one fma correction.  This script
-  replays those binary32 operations in exact arithmetic for every fp16 gate and checks
-  S against the definition; only g <= -88.75 (where exp(-g) overflows binary32, S = -0)
-  and g = -0 (S = -0) need the kernel's closed forms.
+* ``kSiluF16``  the same step sequence for every fp16 gate with a non-trivial result,
+  indexed by |bits| (positive gates, entries [0, F16_POS)) and F16_POS + |bits| (negative
+  gates, |bits| <= 0x558C, i.e. g >= -88.75).  Outside the table the sequence has closed
+  forms: S = g for positive gates from F16_POS on (exp(-g) is below half an ulp of 1, so
+  D = 1), and S = -0 for g <= -88.75 (exp(-g) overflows binary32), which is also the
+  table's last entry, so a kernel can clamp the negative index to it.
 * ``kSiluBf16``  the full binary32 step sequence E = RN(exp(-g)), D = RN(1 + E),
   S = RN(g / D) for every bf16 g whose exponent field lies in [102, 133]
   (2^-25 <= |g| < 128), indexed by (sign, bits & 0x7FFF): 4096 entries per sign.  Outside that range the
@@ -23,20 +19,19 @@ double-precision evaluation:
   g <= -128), which this script checks for every bf16 value.
 
 Values come from mpmath at 160 bits, rounded to binary32 by exact comparison; the
-binary32 steps use numpy (IEEE).  Run from anywhere:
+binary32 steps use numpy (IEEE).  Every finite 16-bit gate is checked, in the table or
+against its closed form.  Run from anywhere:
     python gen_silu_tables.py [output path]
 """
-import math
 import os
 import sys
-from fractions import Fraction
 
 import mpmath
 import numpy as np
 
 F32 = np.float32
 mpmath.mp.prec = 160
-F16_OVERFLOW_BITS = 0x558C      # fp16 88.75: from x = -g >= 88.75 on, exp(x) overflows binary32
+F16_OVERFLOW_BITS = 0x558C      # fp16 88.75: from -g >= 88.75 on, exp(-g) overflows binary32
 BF16_FIELD_LO, BF16_FIELD_HI = 102, 133
 BF16_SPAN = (BF16_FIELD_HI - BF16_FIELD_LO + 1) * 128   # entries per sign
 
@@ -76,111 +71,30 @@ def fmt_table(name: str, ws: list, comment: str) -> str:
     return "\n".join(lines) + "\n"
 
 
-def rn32_exact(v: Fraction) -> float:
-    """Nearest binary32 (ties to even) to an exact rational, with subnormals and overflow."""
-    if v == 0:
-        return 0.0
-    s = -1.0 if v < 0 else 1.0
-    a = abs(v)
-    e = a.numerator.bit_length() - a.denominator.bit_length()
-    while Fraction(2) ** e > a:
-        e -= 1
-    while Fraction(2) ** (e + 1) <= a:
-        e += 1
-    ulp = Fraction(2) ** (max(e, -126) - 23)
-    q = a / ulp
-    n = q.numerator // q.denominator
-    r = q - n
-    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1):
-        n += 1
-    res = n * ulp
-    return s * math.inf if res >= Fraction(2) ** 128 else s * float(res)
+def fp16_gates() -> np.ndarray:
+    """Every fp16 bit pattern's value as binary32 (exact), indexed by the pattern."""
+    return np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float32)
 
 
-def mpf_fraction(v) -> Fraction:
-    man, ex = v.man_exp
-    return Fraction(int(man)) * Fraction(2) ** int(ex)
-
-
-def hi_lo_exact(v):
-    """(RN(v), RN(v - RN(v))) of an mpmath value, both binary32; (inf, 0) on overflow."""
-    fv = mpf_fraction(v)
-    h = rn32_exact(fv)
-    if not math.isfinite(h):
-        return math.inf, 0.0
-    return h, rn32_exact(fv - Fraction(h))
-
-
-def fp16_value(bits: int) -> float:
-    return float(np.array([bits], dtype=np.uint16).view(np.float16)[0])
-
-
-def f16_tables():
-    """The two exp tables of the fp16 path, as lists of (hi, lo) pairs."""
-    ta = [(0.0, 0.0)] * 2048
-    tb = [(0.0, 0.0)] * 2048
-    for sx in (0, 1):
-        for ex in range(31):
-            for m5 in range(32):
-                top = (sx << 15) | (ex << 10) | (m5 << 5)
-                ta[top >> 5] = hi_lo_exact(mpmath.exp(mpmath.mpf(fp16_value(top))))
-                x_lo = (-1 if sx else 1) * m5 * Fraction(2) ** (max(ex, 1) - 25)
-                tb[(sx << 10) | (ex << 5) | m5] = hi_lo_exact(mpmath.exp(mpmath.mpf(x_lo.numerator) / x_lo.denominator))
-    return ta, tb
-
-
-def check_f16_path(ta, tb) -> None:
-    """Replay the kernel's binary32 operations exactly for every finite fp16 gate."""
-    def fin(*v):
-        return all(math.isfinite(x) for x in v)
-
-    def mul(a, b):
-        return rn32_exact(Fraction(a) * Fraction(b)) if fin(a, b) else math.nan
-
-    def fma(a, b, c):
-        return rn32_exact(Fraction(a) * Fraction(b) + Fraction(c)) if fin(a, b, c) else math.nan
-
-    def add(a, b):
-        return rn32_exact(Fraction(a) + Fraction(b)) if fin(a, b) else math.nan
-
-    for h in range(65536):
-        g = fp16_value(h)
-        if not math.isfinite(g):
-            continue
-        if g == 0:
-            want = g / 2
-        else:
-            e = rn32_exact(mpf_fraction(mpmath.exp(-mpmath.mpf(g))))
-            d = add(1.0, e) if math.isfinite(e) else math.inf
-            want = rn32_exact(Fraction(g) / Fraction(d)) if math.isfinite(d) else math.copysign(0.0, g)
-        hx = h ^ 0x8000
-        if hx < 0x8000 and hx >= F16_OVERFLOW_BITS:
-            got = -0.0                                    # closed form: exp(-g) overflows
-        elif (h & 0x7FFF) == 0:
-            got = g                                       # closed form: +-0 keeps its sign
-        else:
-            ah, al = ta[hx >> 5]
-            bh, bl = tb[((hx >> 5) & 0x7E0) | (hx & 0x1F)]
-            p = mul(ah, bh)
-            t = fma(ah, bh, -p)
-            t = fma(al, bh, t)
-            t = fma(ah, bl, t)
-            d = add(1.0, add(p, t))
-            r = rn32_exact(Fraction(1) / Fraction(d))
-            q0 = mul(g, r)
-            res = fma(-q0, d, g)
-            got = fma(res, r, q0)
-        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), \
-            (hex(h), g, got, want)
-
-
-def pair_words(pairs) -> list:
-    return [int(w) for hl in pairs for w in np.array(hl, dtype=np.float32).view(np.uint32)]
+def f16_table():
+    """(F16_POS, table) of the fp16 path; asserts every closed form it relies on."""
+    gates = fp16_gates()
+    s = np.array([silu_steps(g) if np.isfinite(g) else F32(0.0) for g in gates], np.float32)
+    bits = s.view(np.uint32)
+    # F16_POS: the first positive |bits| from which S = g for every finite positive gate
+    pos = 0x7C00
+    while pos > 0 and bits[pos - 1] == gates[pos - 1].view(np.uint32):
+        pos -= 1
+    assert 0x4000 < pos < 0x5000, hex(pos)                        # g near 16.6
+    neg = np.arange(0x8000, 0x8000 + F16_OVERFLOW_BITS + 1)
+    assert np.all(np.isfinite(gates[neg]))
+    assert np.all(bits[0x8000 + F16_OVERFLOW_BITS:0xFC00] == 0x80000000)   # -0 from -88.75 on
+    assert bits[0x8000 + F16_OVERFLOW_BITS - 1] != 0x80000000              # but not before
+    return pos, np.concatenate([s[:pos], s[neg]])
 
 
 def main(out_path: str) -> None:
-    ta, tb = f16_tables()
-    check_f16_path(ta, tb)
+    f16_pos, f16 = f16_table()
 
     bits = np.arange(65536, dtype=np.uint32)
     gates = (bits << 16).view(np.float32)
@@ -209,12 +123,12 @@ def main(out_path: str) -> None:
         f"#define PTGQ_SILU_BF16_FIELD_LO {BF16_FIELD_LO}",
         f"#define PTGQ_SILU_BF16_FIELD_HI {BF16_FIELD_HI}",
         f"#define PTGQ_SILU_BF16_SPAN {BF16_SPAN}",
+        f"#define PTGQ_SILU_F16_POS 0x{f16_pos:04X}",
         f"#define PTGQ_SILU_F16_OVERFLOW_BITS 0x{F16_OVERFLOW_BITS:04X}",
+        f"#define PTGQ_SILU_F16_ENTRIES {len(f16)}",
         "",
-        fmt_table("kSiluF16A", pair_words(ta),
-                  "exp(x_hi) as (hi, lo) pairs, x_hi = fp16 x = -g with its low 5 mantissa bits cleared, [bits(x) >> 5]"),
-        fmt_table("kSiluF16B", pair_words(tb),
-                  "exp(x_lo) as (hi, lo) pairs, x_lo = the low 5 mantissa bits of x, [sign][exponent][low 5 bits]"),
+        fmt_table("kSiluF16", words(f16),
+                  "binary32 silu(g) for fp16 g: [|bits|] (g >= 0, |bits| < POS), [POS + |bits|] (g < 0)"),
         fmt_table("kSiluBf16", words(table),
                   "binary32 silu(g) for bf16 g, [sign][bits & 0x7FFF - (FIELD_LO << 7)]"),
     ]

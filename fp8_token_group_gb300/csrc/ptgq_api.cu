@@ -121,10 +121,12 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
-std::map<std::tuple<const void*, int, size_t>, int> g_occupancy;   // (kernel, device, smem)
+// (kernel, device, smem): each kernel is always launched with the same CTA size
+std::map<std::tuple<const void*, int, size_t>, int> g_occupancy;
 std::map<std::pair<const void*, int>, size_t> g_smem_attr;          // (kernel, device) -> max set
 
-int launch_blocks(const void* fn, int dev, size_t smem, int* blocks_per_sm, int* sm_count) {
+int launch_blocks(const void* fn, int dev, size_t smem, int threads, int* blocks_per_sm,
+                  int* sm_count) {
   std::lock_guard<std::mutex> lock(g_mu);
   auto it = g_devices.find(dev);
   if (it == g_devices.end()) {
@@ -148,7 +150,7 @@ int launch_blocks(const void* fn, int dev, size_t smem, int* blocks_per_sm, int*
   auto ot = g_occupancy.find(okey);
   if (ot == g_occupancy.end()) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kThreads, smem) != cudaSuccess || nb < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess || nb < 1) {
       cudaGetLastError();
       return PTGQ_ERR_CUDA;
     }
@@ -213,8 +215,10 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   const size_t smem = dynamic_smem_bytes(key, masked ? n : 0);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PTGQ_ERR_CUDA;
+  const int threads = quant_threads(key.fp16 != 0, key.silu != 0);
+  const int warps = threads / 32;
   int per_sm = 0, sms = 0;
-  rc = launch_blocks(fn, dev, smem, &per_sm, &sms);
+  rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
   if (rc != PTGQ_OK) return rc;
 
   // Persistent grid: at most one full wave, fewer when the work is small (masked: as
@@ -228,20 +232,20 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   if (!masked && !fuse_silu && tasks <= 8 * static_cast<int64_t>(per_sm) * sms * kWarps) {
     key.light = 1;
     fn = kernel_for(key);
-    rc = launch_blocks(fn, dev, smem, &per_sm, &sms);
+    rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
     if (rc != PTGQ_OK) return rc;
   }
-  int64_t want = (tasks + kWarps - 1) / kWarps;
+  int64_t want = (tasks + warps - 1) / warps;
   if (!masked) {
     const int64_t zero_chunks = (p.zero_q_end - p.zero_q_begin) / 16 + p.zero_s_rows * g.ncol;
-    want = std::max<int64_t>(want, (zero_chunks + kThreads - 1) / kThreads);
+    want = std::max<int64_t>(want, (zero_chunks + threads - 1) / threads);
   }
   const int64_t full = static_cast<int64_t>(per_sm) * sms;
   const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, full)));
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];

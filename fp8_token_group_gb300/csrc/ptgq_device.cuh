@@ -92,12 +92,14 @@ __device__ __forceinline__ uint32_t udiv(uint32_t n, uint32_t d, uint32_t magic)
   return q;
 }
 
-// Exclusive prefix sum over clamp(masked_m[e], 0, rows), e < n, into prefix[0..n].
+// Exclusive prefix sum over clamp(masked_m[e], 0, rows), e < n, into prefix[0..n], by a
+// CTA of kT threads.
+template <int kT = kThreads>
 __device__ __forceinline__ void masked_prefix(const int32_t* __restrict__ masked_m, int64_t n,
                                               int64_t rows, int32_t* prefix) {
-  __shared__ int32_t warp_tot[kWarps];
+  __shared__ int32_t warp_tot[kT / 32];
   const int tid = threadIdx.x;
-  const int chunk = static_cast<int>((n + kThreads - 1) / kThreads);
+  const int chunk = static_cast<int>((n + kT - 1) / kT);
   const int lo = tid * chunk;
   const int hi = min(lo + chunk, static_cast<int>(n));
   int32_t local = 0;
@@ -122,7 +124,7 @@ __device__ __forceinline__ void masked_prefix(const int32_t* __restrict__ masked
     const int32_t m = masked_m[e];
     run += m < 0 ? 0 : (m > rows ? static_cast<int32_t>(rows) : m);
   }
-  if (tid == kThreads - 1) prefix[n] = base + incl;
+  if (tid == kT - 1) prefix[n] = base + incl;
 }
 
 // Rows-to-expert buckets for the masked scheduler: bucket[b] is the expert of live row
@@ -145,9 +147,10 @@ __device__ __forceinline__ uint32_t bucket_shift(uint32_t live) {
   return bits > 8 ? static_cast<uint32_t>(bits - 8) : 0u;
 }
 
+template <int kT = kThreads>
 __device__ __forceinline__ void build_buckets(const int32_t* prefix, int n, uint32_t live,
                                               uint32_t shift, int32_t* bucket) {
-  for (int b = threadIdx.x; b <= kBuckets; b += kThreads) {
+  for (int b = threadIdx.x; b <= kBuckets; b += kT) {
     const uint32_t r0 = min(static_cast<uint32_t>(b) << shift, live > 0u ? live - 1u : 0u);
     bucket[b] = expert_in(prefix, 0, n - 1, r0);
   }
@@ -242,13 +245,14 @@ __device__ __forceinline__ float div_by_const(float a, float d, float rd) {
   return __fmaf_rn(e, rd, q0);
 }
 
-// Copy `n16` 16-byte chunks of module constants into shared memory with cp.async: every
-// thread issues all its chunks before waiting, so the copy costs one L2 round trip.  The
-// caller synchronizes the block afterwards.
+// Copy `n16` 16-byte chunks of module constants into shared memory with cp.async, by a
+// CTA of kT threads: every thread issues all its chunks before waiting, so the copy costs
+// one L2 round trip.  The caller synchronizes the block afterwards.
+template <int kT = kThreads>
 __device__ __forceinline__ void copy_to_smem_async(void* dst, const void* src, int n16) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   const char* s = static_cast<const char*>(src);
-  for (int i = threadIdx.x; i < n16; i += kThreads)
+  for (int i = threadIdx.x; i < n16; i += kT)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + 16u * i), "l"(s + 16 * i)
                  : "memory");
   asm volatile("cp.async.commit_group;" ::: "memory");

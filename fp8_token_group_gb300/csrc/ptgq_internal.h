@@ -7,8 +7,16 @@
 
 namespace ptgq {
 
-constexpr int kThreads = 256;                 // 8 warps per CTA
+constexpr int kThreads = 256;                 // 8 warps per CTA (all but the fp16 silu instances)
 constexpr int kWarps = kThreads / 32;
+#ifndef PTGQ_TUNE_F16_SILU_THREADS
+#define PTGQ_TUNE_F16_SILU_THREADS 1024
+#endif
+// Threads per CTA of a quantizer instance.  The fp16 fused-silu instances hold a 162 KB
+// table of silu results in shared memory, so one CTA per SM carries all their warps.
+constexpr int quant_threads(bool fp16, bool silu) {
+  return fp16 && silu ? PTGQ_TUNE_F16_SILU_THREADS : kThreads;
+}
 constexpr int kMaxExperts = 4096;             // masked scheduler: E <= kMaxExperts
 constexpr int kBuckets = 256;                 // masked scheduler: row-to-expert buckets
 

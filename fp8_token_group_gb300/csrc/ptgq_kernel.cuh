@@ -32,13 +32,12 @@
 
 namespace ptgq {
 
-constexpr int kSiluF16Words = 2 * 2 * 2048;          // tables A and B, (hi, lo) pairs
+constexpr int kSiluF16Words = (PTGQ_SILU_F16_ENTRIES + 3) / 4 * 4;
 constexpr int kSiluBf16Words = 2 * PTGQ_SILU_BF16_SPAN;
 
 template <bool kFp16, bool kSilu>
 struct SmemTables {
-  // bf16 silu reads the precomputed table of results; fp16 silu forms exp(-g) from the
-  // two tables of its split exponent.
+  // The fused-silu instances read precomputed binary32 silu results from shared memory.
   static constexpr int words = !kSilu ? 0 : (kFp16 ? kSiluF16Words : kSiluBf16Words);
   static constexpr int bytes = (words * 4 + 15) / 16 * 16;
 };
@@ -55,11 +54,18 @@ struct Slot {
 // the next batch's loads are issued before the current batch is computed, and the CTAs per
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
 // CTAs/SM (64 registers).  bf16 silu, 3 CTAs/SM: flat one task pipelined, masked two tasks
-// loaded then computed.  fp16 silu, 3 CTAs/SM: one task, not pipelined (its exponential
-// from two tables and its division keep the instance issue-bound).  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE / _MIN_BLOCKS override all
-// instances (sweeps).
+// loaded then computed.  fp16 silu: one CTA of quant_threads() per SM (its table fills most
+// of the shared memory), one task pipelined.  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE /
+// _MIN_BLOCKS override all bf16-silu and plain instances, PTGQ_TUNE_F16_SILU_BATCH /
+// _PIPELINE the fp16 silu ones (sweeps).
 #ifndef PTGQ_TUNE_SILU_BATCH
 #define PTGQ_TUNE_SILU_BATCH 1
+#endif
+#ifndef PTGQ_TUNE_F16_SILU_BATCH
+#define PTGQ_TUNE_F16_SILU_BATCH 1
+#endif
+#ifndef PTGQ_TUNE_F16_SILU_PIPELINE
+#define PTGQ_TUNE_F16_SILU_PIPELINE 1
 #endif
 // The light flavour of the plain flat instances (kLight): one task per batch at 6 CTAs/SM
 // (40 registers, 48 warps per SM).  It ramps up faster when each warp has only a few
@@ -69,14 +75,18 @@ struct Slot {
 template <bool kFp16, bool kSilu, bool kMasked, bool kLight = false>
 struct Tuning {
   static_assert(!kLight || (!kSilu && !kMasked), "the light flavour is plain flat only");
+  static constexpr bool f16_silu = kFp16 && kSilu;
+  static constexpr int threads = quant_threads(kFp16, kSilu);
 #ifdef PTGQ_TUNE_BATCH
-  static constexpr int batch = kSilu ? PTGQ_TUNE_SILU_BATCH : PTGQ_TUNE_BATCH;
-  static constexpr bool pipeline = PTGQ_TUNE_PIPELINE;
-  static constexpr int min_blocks = PTGQ_TUNE_MIN_BLOCKS;
+  static constexpr int batch = f16_silu ? PTGQ_TUNE_F16_SILU_BATCH
+                                        : (kSilu ? PTGQ_TUNE_SILU_BATCH : PTGQ_TUNE_BATCH);
+  static constexpr bool pipeline = f16_silu ? PTGQ_TUNE_F16_SILU_PIPELINE : PTGQ_TUNE_PIPELINE;
+  static constexpr int min_blocks = f16_silu ? 1 : PTGQ_TUNE_MIN_BLOCKS;
 #else
-  static constexpr int batch = (kLight || (kSilu && (kFp16 || !kMasked))) ? 1 : 2;
-  static constexpr bool pipeline = kSilu && !kFp16 && !kMasked;
-  static constexpr int min_blocks = kLight ? 6 : (!kSilu ? 4 : 3);
+  static constexpr int batch =
+      f16_silu ? PTGQ_TUNE_F16_SILU_BATCH : ((kLight || (kSilu && !kMasked)) ? 1 : 2);
+  static constexpr bool pipeline = f16_silu ? PTGQ_TUNE_F16_SILU_PIPELINE : (kSilu && !kMasked);
+  static constexpr int min_blocks = f16_silu ? 1 : (kLight ? 6 : (!kSilu ? 4 : 3));
 #endif
 };
 
@@ -84,7 +94,8 @@ struct Tuning {
 // the element quotients taken by approximate division (fast-math interop).  The scale
 // format is a template parameter so that only the packed instances carry the exponent OR.
 template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked, bool kLight = false>
-__global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLight>::min_blocks))
+__global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::threads),
+                                  (Tuning<kFp16, kSilu, kMasked, kLight>::min_blocks))
     quant_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr bool kPow2 = kFmt == 1 || kFmt == 2;
@@ -92,16 +103,14 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
   using Tab = SmemTables<kFp16, kSilu>;
   using Tune = Tuning<kFp16, kSilu, kMasked, kLight>;
   constexpr int kB = Tune::batch;
+  constexpr int kT = Tune::threads;
+  constexpr int kW = kT / 32;
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Tab::bytes);
 
   // Module constants first (asynchronously): they do not depend on the previous grid.
   if constexpr (kSilu) {
-    if constexpr (kFp16) {
-      copy_to_smem_async(smem, kSiluF16A, kSiluF16Words / 8);
-      copy_to_smem_async(smem + 2 * kSiluF16Words, kSiluF16B, kSiluF16Words / 8);
-    } else {
-      copy_to_smem_async(smem, kSiluBf16, kSiluBf16Words / 4);
-    }
+    if constexpr (kFp16) copy_to_smem_async<kT>(smem, kSiluF16, kSiluF16Words / 4);
+    else copy_to_smem_async<kT>(smem, kSiluBf16, kSiluBf16Words / 4);
   }
 
   griddep_wait();
@@ -111,21 +120,22 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
   int32_t* bucket = prefix + (p.n + 1);
   uint32_t bshift = 0u;
   if constexpr (kMasked) {
-    masked_prefix(p.masked_m, p.n, p.rows, prefix);
+    masked_prefix<kT>(p.masked_m, p.n, p.rows, prefix);
     __syncthreads();
     // A grid sized without knowing the live counts (no hint) often has CTAs with no task:
     // they return here, before the row-to-expert buckets (the condition is uniform).
     const uint32_t live = static_cast<uint32_t>(prefix[p.n]);
     const uint32_t upw_log2 = 5u - (p.lg_log2 + p.ug_log2);
     const uint32_t tasks = (live * p.upr + (1u << upw_log2) - 1u) >> upw_log2;
-    if (blockIdx.x * kWarps >= tasks) {
+    if (blockIdx.x * kW >= tasks) {
       if constexpr (kSilu) copy_to_smem_wait();    // no copy outlives its CTA
       return;
     }
     bshift = bucket_shift(live);
-    build_buckets(prefix, static_cast<int>(p.n), live, bshift, bucket);
+    build_buckets<kT>(prefix, static_cast<int>(p.n), live, bshift, bucket);
   }
-  if constexpr (kSilu) copy_to_smem_wait();
+  // A pipelined instance waits for its table only once its first loads are in flight.
+  if constexpr (kSilu && !Tune::pipeline) copy_to_smem_wait();
   __syncthreads();
   const uint32_t total_units = masked ? static_cast<uint32_t>(prefix[p.n]) * p.upr : p.units_flat;
 
@@ -140,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
   const uint32_t kk = local & (lg - 1u);                     // lane within the group
   const uint32_t G = 16u << p.lg_log2;
   const uint32_t total_tasks = (total_units + (1u << upw_log2) - 1u) >> upw_log2;
-  const uint32_t stride = gridDim.x * kWarps;
+  const uint32_t stride = gridDim.x * kW;
   const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
   uint8_t* __restrict__ q = static_cast<uint8_t*>(p.q);
   const float* silu_tab = reinterpret_cast<const float*>(smem);
@@ -182,12 +192,12 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
     uint32_t amax_bits;
     if constexpr (kSilu) {
       if constexpr (kFp16) {
-        const float2* ta = reinterpret_cast<const float2*>(silu_tab);
-        const float2* tb = ta + 2048;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float s0 = silu_f16(a.w[i] & 0xFFFFu, ta, tb, PTGQ_SILU_F16_OVERFLOW_BITS);
-          const float s1 = silu_f16(a.w[i] >> 16, ta, tb, PTGQ_SILU_F16_OVERFLOW_BITS);
+          const float s0 = silu_f16(a.w[i] & 0xFFFFu, silu_tab, PTGQ_SILU_F16_POS,
+                                    PTGQ_SILU_F16_ENTRIES);
+          const float s1 = silu_f16(a.w[i] >> 16, silu_tab, PTGQ_SILU_F16_POS,
+                                    PTGQ_SILU_F16_ENTRIES);
           v[i] = mul2(pk2(s0, s1), widen2<true>(b.w[i]));
         }
       } else {
@@ -313,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
   // Batches of KB tasks: all their loads are issued, then all are computed.
   auto batches = [&](auto kb) {
     constexpr int KB = decltype(kb)::value;
-    for (uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < total_tasks; t += KB * stride) {
+    for (uint32_t t = blockIdx.x * kW + (threadIdx.x >> 5); t < total_tasks; t += KB * stride) {
       Slot cur[KB];
       Raw16 ca[KB], cb[KB];
 #pragma unroll
@@ -329,11 +339,15 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
     if (kB > 1 && total_tasks <= stride) batches(std::integral_constant<int, 1>{});
     else batches(std::integral_constant<int, kB>{});
   } else if (total_units > 0u) {
-    uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    uint32_t t = blockIdx.x * kW + (threadIdx.x >> 5);
     Slot cur[kB];
     Raw16 ca[kB], cb[kB];
 #pragma unroll
     for (int i = 0; i < kB; ++i) issue(t + i * stride, cur[i], ca[i], cb[i]);
+    if constexpr (kSilu) {          // uniform: every thread reaches this barrier
+      copy_to_smem_wait();
+      __syncthreads();
+    }
     while (t < total_tasks) {
       Slot nxt[kB];
       Raw16 na[kB], nb[kB];
@@ -351,10 +365,12 @@ __global__ void __launch_bounds__(kThreads, (Tuning<kFp16, kSilu, kMasked, kLigh
     }
   }
 
+  if constexpr (kSilu && Tune::pipeline) copy_to_smem_wait();   // no copy outlives its CTA
+
   // Flat scheduler: zero the padding rows of out_q and of the scales.
   if constexpr (!kMasked) {
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kT + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * kT;
     for (int64_t off = p.zero_q_begin + tid * 16; off < p.zero_q_end; off += nthr * 16)
       st_128(q + off, 0u, 0u, 0u, 0u);
     const int64_t nz = p.zero_s_rows * p.s_ncol;

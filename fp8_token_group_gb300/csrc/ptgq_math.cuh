@@ -41,33 +41,19 @@ PTGQ_HD uint32_t f2u(float f) {
 
 // silu(g) = g / (1 + exp(-g)) with the binary32 step sequence E = RN(exp(-g)),
 // D = RN(1 + E), S = RN(g / D) (sglang PR #30924, "Implementation breakdown" item 1: the
-// fused silu_and_mul trait), for an fp16 gate g given by its bits h.  With x = -g,
-// exp(x) = exp(x_hi) * exp(x_lo): x_hi keeps the sign, exponent and top five mantissa bits
-// of x, x_lo the rest.  Table A holds exp(x_hi) at [bits(x) >> 5], table B exp(x_lo) at
-// [sign][exponent][low five bits], each as a (hi, lo) binary32 pair.  E is their product
-// in double-float, rounded once; S = RN(g / D) from the correctly rounded reciprocal r and
-// one fma correction (q0 = RN(g r), q = RN(q0 + (g - q0 D) r)).  The generator of the
-// tables replays these operations in exact arithmetic for every fp16 gate: the result is
-// S exactly, except for two closed forms, g <= -88.75 (exp(-g) overflows binary32, so
-// S = -0) and g = -0 (S = -0).
-__device__ __forceinline__ float silu_f16(uint32_t h, const float2* ta, const float2* tb,
-                                          uint32_t overflow_bits) {
+// fused silu_and_mul trait), for an fp16 gate g given by its bits h, read from the
+// precomputed table of binary32 results: entry |h| for a positive gate, pos + |h| for a
+// negative one.  The table holds every non-trivial result.  Positive gates from |h| = pos
+// on (g >= 16.64) have S = g, since E is below half an ulp of 1.  Negative gates end at
+// entry entries - 1 (g = -88.75, from which on exp(-g) overflows binary32), whose value is
+// the -0 of every gate beyond, so the clamp of the index returns it.  Every index lies
+// inside the table for any 16-bit h.
+__device__ __forceinline__ float silu_f16(uint32_t h, const float* table, uint32_t pos,
+                                          uint32_t entries) {
+  const uint32_t idx = min((h & 0x7FFFu) + (h >> 15) * pos, entries - 1u);
+  const float tv = table[idx];
   const float g = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-  const uint32_t hx = h ^ 0x8000u;                                     // bits of x = -g
-  const float2 a = ta[hx >> 5];
-  const float2 b = tb[((hx >> 5) & 0x7E0u) | (hx & 0x1Fu)];
-  const float p = __fmul_rn(a.x, b.x);
-  float t = __fmaf_rn(a.x, b.x, -p);
-  t = __fmaf_rn(a.y, b.x, t);
-  t = __fmaf_rn(a.x, b.y, t);
-  const float d = __fadd_rn(1.0f, __fadd_rn(p, t));
-  const float r = __frcp_rn(d);
-  const float q0 = __fmul_rn(g, r);
-  const float res = __fmaf_rn(-q0, d, g);
-  float s = __fmaf_rn(res, r, q0);
-  s = (h & 0x7FFFu) == 0u ? g : s;
-  s = (hx < 0x8000u && hx >= overflow_bits) ? -0.0f : s;
-  return s;
+  return h - pos < 0x8000u - pos ? g : tv;          // 0 <= g with |h| >= pos
 }
 
 // The same sequence for a bf16 gate, read from the precomputed table of binary32

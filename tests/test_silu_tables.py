@@ -1,8 +1,8 @@
 """The GPU kernels' silu tables (fp8_token_group_gb300/csrc/silu_tables.inc) are generated
-data.  Regenerating them re-runs the generator's own checks: the bf16 closed forms outside
-the table for every bf16 gate, and an exact replay of the fp16 path's binary32 operations
-for every fp16 gate.  The committed file must then match the regenerated one byte for byte.
-CPU only; no kernel runs."""
+data.  Regenerating them re-runs the generator's own checks: the closed forms outside each
+table (S = g/2, g or -0 for bf16; S = g or -0 for fp16) for every 16-bit gate of both types.
+The committed file must then match the regenerated one byte for byte.  CPU only; no kernel
+runs."""
 import importlib.util
 import os
 
@@ -12,7 +12,6 @@ CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                     "fp8_token_group_gb300", "csrc")
 
 
-@pytest.mark.slow
 def test_committed_silu_tables_regenerate_identically(tmp_path):
     pytest.importorskip("mpmath")
     spec = importlib.util.spec_from_file_location("gen_silu_tables",
