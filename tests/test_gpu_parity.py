@@ -290,6 +290,9 @@ def test_flat_zero_tokens_only_zero_fills_padding():
     for fmt in FMTS:
         for layout in LAYOUTS:
             compare(x, Case(scale_fmt=fmt, layout=layout, tokens_pad=9))
+    # the silu instances copy their table before they know there is no task
+    for dt in (torch.bfloat16, torch.float16):
+        compare(torch.zeros((0, 2048), dtype=dt), Case(silu=True, tokens_pad=9))
 
 
 def test_masked_all_empty_and_zero_experts():
@@ -442,7 +445,9 @@ def test_binding_rejects_short_buffers_before_launch():
 
 def test_masked_4096_experts_mostly_empty():
     """The largest expert count, with many empty and one-row experts: exercises the
-    row-to-expert buckets across runs of empty experts."""
+    row-to-expert buckets across runs of empty experts.  With fused silu on fp16 input it is
+    also the largest shared-memory footprint: the fp16 silu table plus 4096 experts' prefix
+    sums and the buckets."""
     E, tp = 4096, 3
     x = synth.normal((E, tp, 256), torch.bfloat16, seed=4)
     g = torch.Generator().manual_seed(11)
@@ -453,6 +458,9 @@ def test_masked_4096_experts_mostly_empty():
         compare(x, Case(scale_fmt=fmt, layout=P.COL_MAJOR_TMA), masked_m=mm.numpy())
     compare(torch.cat([x, x], 2), Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED,
                                        layout=P.COL_MAJOR_TMA), masked_m=mm.numpy())
+    xh = synth.normal((E, tp, 512), torch.float16, seed=6)
+    compare(xh, Case(silu=True, scale_fmt=P.SCALE_UE8M0_PACKED, layout=P.COL_MAJOR_TMA),
+            masked_m=mm.numpy())
 
 
 def test_pinned_host_buffers_in_place():
