@@ -25,6 +25,11 @@ __device__ __forceinline__ void ld_stream_256(Raw16& v, const void* p) {
                : "l"(p));
 }
 
+// Brings the line holding p into L2 (no register result; the address must be valid).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void st_128(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");

@@ -77,6 +77,10 @@ struct Tuning {
   static_assert(!kLight || (!kSilu && !kMasked), "the light flavour is plain flat only");
   static constexpr bool f16_silu = kFp16 && kSilu;
   static constexpr int threads = quant_threads(kFp16, kSilu);
+  // Masked calls with an expected_m hint prefetch their guessed first rows (hinted decode
+  // batch, bf16 silu: 3.16 -> 2.91 us).  Not the fp16 silu instances: their table copy, not
+  // the row loads, is what they wait for (4.79 -> 4.88 us with the prefetch).
+  static constexpr bool hint_prefetch = !f16_silu;
 #ifdef PTGQ_TUNE_BATCH
   static constexpr int batch = f16_silu ? PTGQ_TUNE_F16_SILU_BATCH
                                         : (kSilu ? PTGQ_TUNE_SILU_BATCH : PTGQ_TUNE_BATCH);
@@ -120,6 +124,29 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   int32_t* bucket = prefix + (p.n + 1);
   uint32_t bshift = 0u;
   if constexpr (kMasked) {
+    // With a hint of the live rows per expert, the rows of this warp's first task, guessed
+    // as if every expert had exactly rows_hint live rows, go to L2 while masked_m is read.
+    // The guess only decides what is prefetched: rows below rows_hint <= rows of experts
+    // below n, so every prefetched address lies inside x.
+    if (Tune::hint_prefetch && p.rows_hint > 0u) {
+      const uint32_t lane = threadIdx.x & 31u;
+      const uint32_t lu_log2 = p.lg_log2 + p.ug_log2;
+      const uint32_t local = lane & ((1u << lu_log2) - 1u);
+      const uint32_t u = ((blockIdx.x * kW + (threadIdx.x >> 5)) << (5u - lu_log2)) +
+                         (lane >> lu_log2);
+      const uint32_t R = udiv(u, p.upr, p.upr_magic);
+      const uint32_t e = udiv(R, p.rows_hint, p.rows_hint_magic);
+      const uint32_t g = ((u - R * p.upr) << p.ug_log2) + (local >> p.lg_log2);
+      if (e < p.n && g < p.ng) {
+        const uint32_t row = R - e * p.rows_hint;
+        const uint16_t* src = static_cast<const uint16_t*>(p.x) +
+                              (static_cast<int64_t>(e) * p.rows + row) * p.in_row +
+                              (static_cast<int64_t>(g) << (4u + p.lg_log2)) +
+                              (local & ((1u << p.lg_log2) - 1u)) * 16u;
+        prefetch_l2(src);
+        if constexpr (kSilu) prefetch_l2(src + p.hidden);
+      }
+    }
     masked_prefix<kT>(p.masked_m, p.n, p.rows, prefix);
     __syncthreads();
     // A grid sized without knowing the live counts (no hint) often has CTAs with no task:

@@ -125,6 +125,20 @@ def test_masked_expected_m_hint_changes_nothing(expected_m):
                     expected_m=expected_m), masked_m=mm.numpy())
 
 
+@pytest.mark.parametrize("G", [16, 32, 64, 128])
+@pytest.mark.parametrize("silu", [False, True])
+def test_masked_hint_every_group_size(G, silu):
+    """A hinted call guesses each warp's first rows (as if every expert had expected_m live
+    rows) and prefetches them before the live counts are read.  The guess must not matter:
+    hints below, at and above the live counts, every group size and scale format."""
+    x = synth.normal((5, 40, 768 * (2 if silu else 1)), torch.bfloat16, seed=31)
+    mm = np.array([3, 0, 40, 3, 17], np.int32)
+    for hint in (1, 3, 64):
+        for fmt in (P.SCALE_FP32, P.SCALE_UE8M0_PACKED):
+            compare(x, Case(group=G, silu=silu, scale_fmt=fmt, layout=P.COL_MAJOR_TMA,
+                            expected_m=hint), masked_m=mm)
+
+
 @pytest.mark.parametrize("fmt", [P.SCALE_UE8M0_PACKED, P.SCALE_FP32])
 def test_masked_large_pad_per_expert(fmt):
     """A prefill-sized masked layout: 8 experts of 4096 rows, live counts up to the pad
