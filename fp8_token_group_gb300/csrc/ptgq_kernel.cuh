@@ -219,12 +219,13 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
     uint32_t amax_bits;
     if constexpr (kSilu) {
       if constexpr (kFp16) {
+        static_assert(PTGQ_SILU_F16_POS + 0x7FFF < 0x10000 && PTGQ_SILU_F16_ENTRIES <= 0x10000,
+                      "packed table indices need 16 bits per half");
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float s0 = silu_f16(a.w[i] & 0xFFFFu, silu_tab, PTGQ_SILU_F16_POS,
-                                    PTGQ_SILU_F16_ENTRIES);
-          const float s1 = silu_f16(a.w[i] >> 16, silu_tab, PTGQ_SILU_F16_POS,
-                                    PTGQ_SILU_F16_ENTRIES);
+          const uint32_t idx = silu_f16_index2(a.w[i], PTGQ_SILU_F16_POS, PTGQ_SILU_F16_ENTRIES);
+          const float s0 = silu_f16_pick(a.w[i] & 0xFFFFu, silu_tab[idx & 0xFFFFu], PTGQ_SILU_F16_POS);
+          const float s1 = silu_f16_pick(a.w[i] >> 16, silu_tab[idx >> 16], PTGQ_SILU_F16_POS);
           v[i] = mul2(pk2(s0, s1), widen2<true>(b.w[i]));
         }
       } else {

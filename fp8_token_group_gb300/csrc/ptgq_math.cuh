@@ -47,13 +47,19 @@ PTGQ_HD uint32_t f2u(float f) {
 // on (g >= 16.64) have S = g, since E is below half an ulp of 1.  Negative gates end at
 // entry entries - 1 (g = -88.75, from which on exp(-g) overflows binary32), whose value is
 // the -0 of every gate beyond, so the clamp of the index returns it.  Every index lies
-// inside the table for any 16-bit h.
-__device__ __forceinline__ float silu_f16(uint32_t h, const float* table, uint32_t pos,
-                                          uint32_t entries) {
-  const uint32_t idx = min((h & 0x7FFFu) + (h >> 15) * pos, entries - 1u);
-  const float tv = table[idx];
+// inside the table for any 16-bit h.  (silu_f16_index2 and silu_f16_pick below.)
+// Both gates of a 32-bit word at once: the table index of each 16-bit half (|h|, plus pos
+// for a negative gate) clamped to entries - 1 with one min.u16x2.  No carry crosses the
+// halves, since |h| + pos < 2^16.
+__device__ __forceinline__ uint32_t silu_f16_index2(uint32_t w, uint32_t pos, uint32_t entries) {
+  uint32_t idx = (w & 0x7FFF7FFFu) + ((w >> 15) & 0x00010001u) * pos;
+  asm("min.u16x2 %0, %0, %1;" : "+r"(idx) : "r"((entries - 1u) * 0x00010001u));
+  return idx;
+}
+// The result for gate bits h from its table entry tv: g itself for 0 <= g with |h| >= pos.
+__device__ __forceinline__ float silu_f16_pick(uint32_t h, float tv, uint32_t pos) {
   const float g = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-  return h - pos < 0x8000u - pos ? g : tv;          // 0 <= g with |h| >= pos
+  return h - pos < 0x8000u - pos ? g : tv;
 }
 
 // The same sequence for a bf16 gate, read from the precomputed table of binary32
