@@ -220,7 +220,6 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PTGQ_ERR_CUDA;
   const int threads = quant_threads(key.fp16 != 0, key.silu != 0);
-  const int warps = threads / 32;
   int per_sm = 0, sms = 0;
   rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
   if (rc != PTGQ_OK) return rc;
@@ -239,7 +238,8 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
     rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
     if (rc != PTGQ_OK) return rc;
   }
-  int64_t want = (tasks + warps - 1) / warps;
+  const int per_cta = quant_small_tasks_per_cta(key.fp16 != 0, key.silu != 0);
+  int64_t want = (tasks + per_cta - 1) / per_cta;
   if (!masked) {
     const int64_t zero_chunks = (p.zero_q_end - p.zero_q_begin) / 16 + p.zero_s_rows * g.ncol;
     want = std::max<int64_t>(want, (zero_chunks + threads - 1) / threads);

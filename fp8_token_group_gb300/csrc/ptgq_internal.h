@@ -17,6 +17,14 @@ constexpr int kWarps = kThreads / 32;
 constexpr int quant_threads(bool fp16, bool silu) {
   return fp16 && silu ? PTGQ_TUNE_F16_SILU_THREADS : kThreads;
 }
+// Tasks a CTA of an instance takes in a call too small to fill the grid: one per warp,
+// except in the fp16 silu instances, whose large CTAs then deal consecutive tasks
+// round-robin over the grid and are given 8 each, so a small call spreads over four times
+// as many SMs (each SM's ingress from memory, not its warps, bounds such a call: a
+// [64, 2x2048] call takes 2.3 us instead of 3.6 us).
+constexpr int quant_small_tasks_per_cta(bool fp16, bool silu) {
+  return fp16 && silu ? 8 : quant_threads(fp16, silu) / 32;
+}
 constexpr int kMaxExperts = 4096;             // masked scheduler: E <= kMaxExperts
 constexpr int kBuckets = 256;                 // masked scheduler: row-to-expert buckets
 

@@ -81,6 +81,12 @@ struct Tuning {
   // batch, bf16 silu: 3.16 -> 2.91 us).  Not the fp16 silu instances: their table copy, not
   // the row loads, is what they wait for (4.79 -> 4.88 us with the prefetch).
   static constexpr bool hint_prefetch = !f16_silu;
+  // Tasks dealt round-robin over the CTAs (consecutive tasks to consecutive CTAs) instead
+  // of in blocks of one per warp, in masked calls and in flat calls with fewer tasks than
+  // warps: see quant_small_tasks_per_cta.  (Large flat calls keep the blocks: 14.8 us
+  // against 15.2 us round-robin for fp16 silu [8192, 2x2048]; masked silu [32, 384,
+  // 2x4096]: 22.9 us round-robin against 23.3 us.)
+  static constexpr bool round_robin = f16_silu;
 #ifdef PTGQ_TUNE_BATCH
   static constexpr int batch = f16_silu ? PTGQ_TUNE_F16_SILU_BATCH
                                         : (kSilu ? PTGQ_TUNE_SILU_BATCH : PTGQ_TUNE_BATCH);
@@ -109,6 +115,11 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   constexpr int kB = Tune::batch;
   constexpr int kT = Tune::threads;
   constexpr int kW = kT / 32;
+  // This warp's first task, round-robin or in blocks per CTA; the warp then strides by all
+  // the grid's warps.
+  auto first_task = [&](bool rr) {
+    return rr ? blockIdx.x + gridDim.x * (threadIdx.x >> 5) : blockIdx.x * kW + (threadIdx.x >> 5);
+  };
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Tab::bytes);
 
   // Module constants first (asynchronously): they do not depend on the previous grid.
@@ -132,7 +143,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
       const uint32_t lane = threadIdx.x & 31u;
       const uint32_t lu_log2 = p.lg_log2 + p.ug_log2;
       const uint32_t local = lane & ((1u << lu_log2) - 1u);
-      const uint32_t u = ((blockIdx.x * kW + (threadIdx.x >> 5)) << (5u - lu_log2)) +
+      const uint32_t u = (first_task(Tune::round_robin) << (5u - lu_log2)) +
                          (lane >> lu_log2);
       const uint32_t R = udiv(u, p.upr, p.upr_magic);
       const uint32_t e = udiv(R, p.rows_hint, p.rows_hint_magic);
@@ -154,7 +165,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
     const uint32_t live = static_cast<uint32_t>(prefix[p.n]);
     const uint32_t upw_log2 = 5u - (p.lg_log2 + p.ug_log2);
     const uint32_t tasks = (live * p.upr + (1u << upw_log2) - 1u) >> upw_log2;
-    if (blockIdx.x * kW >= tasks) {
+    if ((Tune::round_robin ? blockIdx.x : blockIdx.x * kW) >= tasks) {
       if constexpr (kSilu) copy_to_smem_wait();    // no copy outlives its CTA
       return;
     }
@@ -178,6 +189,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   const uint32_t G = 16u << p.lg_log2;
   const uint32_t total_tasks = (total_units + (1u << upw_log2) - 1u) >> upw_log2;
   const uint32_t stride = gridDim.x * kW;
+  const uint32_t first = first_task(Tune::round_robin && (kMasked || total_tasks < stride));
   const uint16_t* __restrict__ x = static_cast<const uint16_t*>(p.x);
   uint8_t* __restrict__ q = static_cast<uint8_t*>(p.q);
   const float* silu_tab = reinterpret_cast<const float*>(smem);
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   // Batches of KB tasks: all their loads are issued, then all are computed.
   auto batches = [&](auto kb) {
     constexpr int KB = decltype(kb)::value;
-    for (uint32_t t = blockIdx.x * kW + (threadIdx.x >> 5); t < total_tasks; t += KB * stride) {
+    for (uint32_t t = first; t < total_tasks; t += KB * stride) {
       Slot cur[KB];
       Raw16 ca[KB], cb[KB];
 #pragma unroll
@@ -367,7 +379,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
     if (kB > 1 && total_tasks <= stride) batches(std::integral_constant<int, 1>{});
     else batches(std::integral_constant<int, kB>{});
   } else if (total_units > 0u) {
-    uint32_t t = blockIdx.x * kW + (threadIdx.x >> 5);
+    uint32_t t = first;
     Slot cur[kB];
     Raw16 ca[kB], cb[kB];
 #pragma unroll
