@@ -77,10 +77,6 @@ struct Tuning {
   static_assert(!kLight || (!kSilu && !kMasked), "the light flavour is plain flat only");
   static constexpr bool f16_silu = kFp16 && kSilu;
   static constexpr int threads = quant_threads(kFp16, kSilu);
-  // Masked calls with an expected_m hint prefetch their guessed first rows (hinted decode
-  // batch, bf16 silu: 3.16 -> 2.91 us).  Not the fp16 silu instances: their table copy, not
-  // the row loads, is what they wait for (4.79 -> 4.88 us with the prefetch).
-  static constexpr bool hint_prefetch = !f16_silu;
   // Tasks dealt round-robin over the CTAs (consecutive tasks to consecutive CTAs) instead
   // of in blocks of one per warp, in masked calls and in flat calls with fewer tasks than
   // warps: see quant_small_tasks_per_cta.  (Large flat calls keep the blocks: 14.8 us
@@ -136,10 +132,11 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   uint32_t bshift = 0u;
   if constexpr (kMasked) {
     // With a hint of the live rows per expert, the rows of this warp's first task, guessed
-    // as if every expert had exactly rows_hint live rows, go to L2 while masked_m is read.
+    // as if every expert had exactly rows_hint live rows, go to L2 while masked_m is read
+    // (hinted decode batch, bf16 silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us).
     // The guess only decides what is prefetched: rows below rows_hint <= rows of experts
     // below n, so every prefetched address lies inside x.
-    if (Tune::hint_prefetch && p.rows_hint > 0u) {
+    if (p.rows_hint > 0u) {
       const uint32_t lane = threadIdx.x & 31u;
       const uint32_t lu_log2 = p.lg_log2 + p.ug_log2;
       const uint32_t local = lane & ((1u << lu_log2) - 1u);
