@@ -1,0 +1,122 @@
+"""Bounds of the kernel's computed indices, on the CPU.  Each test restates one piece of the
+index arithmetic of fp8_token_group_gb300/csrc/ptgq_kernel.cuh and ptgq_math.cuh with
+numpy and checks, over every 16-bit value or a sweep of launch parameters, that every
+shared-memory or global address it forms lies inside its buffer and equals the plain
+per-element index.  They cover the three places where an index is computed from data or
+from a guess rather than from the loop counters: the bf16 silu table offsets (formed for
+both gates of a word at once, behind a range test), the fp16 silu table indices (two per
+word, clamped with min.u16x2), and the rows prefetched on an expected_m hint.  No kernel
+runs."""
+import itertools
+import os
+import re
+
+import numpy as np
+
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                    "fp8_token_group_gb300", "csrc")
+
+
+def _defs():
+    with open(os.path.join(CSRC, "silu_tables.inc")) as f:
+        text = f.read()
+    return {m.group(1): int(m.group(2), 0)
+            for m in re.finditer(r"#define (PTGQ_SILU_\w+) (\S+)", text)}
+
+
+def _words(lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
+    return (lo.astype(np.uint64) | (hi.astype(np.uint64) << 16)).astype(np.uint32)
+
+
+# Partner halves: each half of a word must come out the same whatever the other half holds.
+PARTNERS = np.array([0x0000, 0x0001, 0x3300, 0x7FFF, 0x8000, 0xB2FF, 0xFFFF], np.uint32)
+
+
+def test_bf16_silu_offsets_behind_the_range_test():
+    """Both gates of a word are offset at once: t = ((w | 0x80008000) - base2) ^ 0x80008000.
+    A half passes the range test when t has no bit at 12 or above in it; the byte offset is
+    then 4 * (sign * SPAN + |h| - base), at most 0x7FFC of the 32 KB table, and a half
+    passes exactly when the gate lies in the table."""
+    d = _defs()
+    base, span = d["PTGQ_SILU_BF16_FIELD_LO"] << 7, d["PTGQ_SILU_BF16_SPAN"]
+    assert span == 4096
+    table_bytes = 2 * span * 4
+    base2 = np.uint32(base | (base << 16))
+    h = np.arange(65536, dtype=np.uint32)
+    mag, sign = h & 0x7FFF, h >> 15
+    in_table = (mag >= base) & (mag < base + span)
+    want = 4 * (sign * span + mag - base)
+    for p in PARTNERS:
+        for w, half in ((_words(h, np.full_like(h, p)), 0), (_words(np.full_like(h, p), h), 1)):
+            t = ((w | np.uint32(0x80008000)) - base2) ^ np.uint32(0x80008000)
+            if half == 0:
+                passes = (t & 0xF000) == 0
+                o = ((t << 2) & 0x3FFC) | ((w >> 1) & 0x4000)
+            else:
+                passes = (t & 0xF0000000) == 0
+                o = ((t >> 14) & 0x3FFC) | ((w >> 17) & 0x4000)
+            assert np.array_equal(passes, in_table)
+            assert np.all(o[passes] <= table_bytes - 4)
+            assert np.array_equal(o[passes], want[passes])
+
+
+def test_fp16_silu_indices_two_per_word():
+    """idx = (w & 0x7FFF7FFF) + ((w >> 15) & 0x00010001) * POS, then min.u16x2 with
+    ENTRIES - 1 in both halves: each half is min(|h| + sign * POS, ENTRIES - 1), inside the
+    table, whatever the other half holds (no carry crosses the halves)."""
+    d = _defs()
+    pos, entries = d["PTGQ_SILU_F16_POS"], d["PTGQ_SILU_F16_ENTRIES"]
+    assert pos + 0x7FFF < 0x10000 and entries <= 0x10000
+    h = np.arange(65536, dtype=np.uint32)
+    want = np.minimum((h & 0x7FFF) + (h >> 15) * pos, entries - 1)
+    for p in PARTNERS:
+        for lo, hi, half in ((h, np.full_like(h, p), 0), (np.full_like(h, p), h, 1)):
+            w = _words(lo, hi)
+            idx = ((w & np.uint32(0x7FFF7FFF)) +
+                   ((w >> 15) & np.uint32(0x00010001)) * np.uint32(pos)).astype(np.uint32)
+            got = np.minimum((idx >> (16 * half)) & 0xFFFF, entries - 1)   # min.u16x2, one half
+            assert np.array_equal(got, want)
+            assert np.all(got < (entries + 3) // 4 * 4)
+
+
+def _udiv(n, d, magic):
+    q = (n * magic) >> 32
+    return q + (n - q * d >= d)
+
+
+def test_hint_prefetch_stays_inside_x():
+    """With an expected_m hint every masked CTA guesses the rows of its warps' first tasks
+    (each expert taken to have min(expected_m, tokens_pad) live rows) and prefetches them.
+    Over shapes, group sizes, scale formats, silu, hints, both task dealings and more warps
+    than tasks, every prefetched 32-byte chunk (gate and, with silu, up) lies inside
+    x = [E, tokens_pad, H_in]."""
+    for E, rows, H, G, packed, silu, hint, rr in itertools.product(
+            [1, 3, 32], [1, 5, 40], [128, 384, 2048], [16, 32, 64, 128], [0, 1], [0, 1],
+            [1, 3, 7, 1000], [0, 1]):
+        if H % G:
+            continue
+        lg_log2 = {16: 0, 32: 1, 64: 2, 128: 3}[G]
+        ug_log2 = 2 if packed else 0
+        ng = H // G
+        upr = (ng + (1 << ug_log2) - 1) >> ug_log2
+        in_row = 2 * H if silu else H
+        rows_hint = min(hint, rows)
+        upr_magic = 0xFFFFFFFF if upr == 1 else (1 << 32) // upr
+        hint_magic = 0xFFFFFFFF if rows_hint <= 1 else (1 << 32) // rows_hint
+        lu = lg_log2 + ug_log2
+        grid, warps = 6, 32 if rr else 8
+        b, w, lane = np.meshgrid(np.arange(grid), np.arange(warps), np.arange(32), indexing="ij")
+        b, w, lane = b.ravel().astype(np.int64), w.ravel().astype(np.int64), lane.ravel()
+        first = b + grid * w if rr else b * warps + w
+        local = lane & ((1 << lu) - 1)
+        u = (first << (5 - lu)) + (lane >> lu)
+        R = _udiv(u, upr, upr_magic)
+        assert np.array_equal(R, u // upr)
+        e = _udiv(R, rows_hint, hint_magic)
+        assert np.array_equal(e, R // rows_hint)
+        g = ((u - R * upr) << ug_log2) + (local >> lg_log2)
+        go = (e < E) & (g < ng)
+        row = R - e * rows_hint
+        off = (e * rows + row) * in_row + (g << (4 + lg_log2)) + (local & ((1 << lg_log2) - 1)) * 16
+        end = off + (H if silu else 0) + 16
+        assert np.all(row[go] < rows) and np.all(end[go] <= E * rows * in_row)
