@@ -108,7 +108,13 @@ float pow2_from_biased(int e) { return bits_to_float(static_cast<uint32_t>(e) <<
 // source snippets": the satfinite conversion saturates instead of producing NaN]),
 // then rounded to the nearest representable value, ties to the even mantissa.
 // The sign is kept, so -0 and negative values that round to zero give 0x80.
+// A NaN quotient (inf / inf: an element that is itself infinite in a group whose amax
+// is infinite) is not clamped: [sglang#30924, "Key source snippets"] clamps with torch,
+// which passes NaN through, and the cast to e4m3fn then gives the format's NaN.  It is
+// encoded 0x7F, with the sign bit clear: IEEE arithmetic leaves the sign of such a NaN
+// open (x86 and NVIDIA GPUs produce opposite default NaNs), so it is not carried.
 uint8_t e4m3_encode(float y) {
+  if (std::isnan(y)) return 0x7F;
   const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
   double a = std::fabs(static_cast<double>(y));
   if (a > 448.0) a = 448.0;
@@ -127,8 +133,11 @@ uint8_t e4m3_encode(float y) {
 }
 
 // int8: round to nearest, ties to even, then clamp to the int8 range
-// [vllm#41326, "Key source snippets": min_8bit / max_8bit kernel bounds].
+// [vllm#41326, "Key source snippets": min_8bit / max_8bit kernel bounds].  A NaN
+// quotient (see e4m3_encode) has no integer value; it is encoded 0, the result of a
+// float-to-integer conversion of NaN on NVIDIA GPUs and of torch's cast to int8.
 int8_t int8_encode(float y) {
+  if (std::isnan(y)) return 0;
   double r = std::nearbyint(static_cast<double>(y));
   if (r > 127.0) r = 127.0;
   if (r < -128.0) r = -128.0;
@@ -299,7 +308,10 @@ static int quant_impl(const uint16_t* x, int in_dtype, int64_t n, int64_t tokens
         float amax = 0.0f;
         for (int64_t i = 0; i < G; ++i) amax = std::fmax(amax, std::fabs(v[i]));
         amax = std::fmax(amax, eps);
-        // 3. scale
+        // 3. scale.  An infinite amax (a silu product that overflows binary32, or an
+        // infinite input) gives s = +inf, and for the UE8M0 formats e = 255 (byte 0xFF),
+        // whose power of two 2^128 is +inf in binary32: every finite element's quotient
+        // is then a signed zero, and an infinite element's is NaN (see e4m3_encode).
         float s = amax / fmax;
         float scale = s;
         int e = 0;
@@ -366,8 +378,12 @@ int oracle_quant_quotient_bound(const uint16_t* x, int in_dtype, int64_t n, int6
 // warp kernel).  For each of the first num_tokens rows:
 //   s   = max_i |x_i| / 448                  (no eps floor)
 //   inv = s == 0 ? 0 : 1 / s                 (an all-zero row gets scale 0, codes 0)
-//   q_i = e4m3(clamp(x_i * inv, -448, 448))  (multiplication by the reciprocal)
-// out_s[r] = s.  Rows of out_q / out_s past num_tokens are not touched (the padded
+//   q_i = e4m3(max(min(x_i * inv, 448), -448))  (multiplication by the reciprocal; the
+//                                               page's clamp, min first, then max)
+// out_s[r] = s.  min and max are IEEE minNum / maxNum (std::fmin / std::fmax, which
+// CUDA's fminf / fmaxf also are): a NaN operand yields the other one.  So when 1/s
+// overflows to +inf (a row whose largest magnitude is below about 1.3e-36), a zero
+// element's product 0 * inf = NaN clamps to +448, and every other element to +-448.  Rows of out_q / out_s past num_tokens are not touched (the padded
 // output contract of the same page).  in_dtype: 0 bf16, 1 fp16, 2 fp32.
 int oracle_per_token_quant(const void* x, int in_dtype, int64_t num_tokens, int64_t hidden,
                            uint8_t* out_q, float* out_s) {
@@ -384,7 +400,7 @@ int oracle_per_token_quant(const void* x, int in_dtype, int64_t num_tokens, int6
     const float inv = s == 0.0f ? 0.0f : 1.0f / s;
     for (int64_t i = 0; i < hidden; ++i) {
       float y = val(i) * inv;
-      y = std::fmin(std::fmax(y, -448.0f), 448.0f);
+      y = std::fmax(std::fmin(y, 448.0f), -448.0f);
       out_q[r * hidden + i] = e4m3_encode(y);
     }
     out_s[r] = s;

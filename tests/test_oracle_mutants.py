@@ -53,6 +53,11 @@ MUTANTS = [
      "const float inv = 1.0f / s;"),
     ("per-token max without abs", "m = std::fmax(m, std::fabs(val(i)));", "m = std::fmax(m, val(i));"),
     ("per-token scale with the wrong FMAX", "const float s = m / 448.0f;", "const float s = m / 480.0f;"),
+    ("per-token clamp with max first", "y = std::fmax(std::fmin(y, 448.0f), -448.0f);",
+     "y = std::fmin(std::fmax(y, -448.0f), 448.0f);"),
+    # NaN quotients (infinite amax)
+    ("e4m3 NaN saturated", "if (std::isnan(y)) return 0x7F;", "if (std::isnan(y)) return 0x7E;"),
+    ("int8 NaN as -128", "if (std::isnan(y)) return 0;", "if (std::isnan(y)) return -128;"),
     # per-token-group -> per-tensor requantization
     ("requant multiplies by the output scale", "const float inv = 1.0f / output_scale;",
      "const float inv = output_scale;"),
@@ -86,6 +91,9 @@ FAST_PINS = [
     npins.test_requant_vs_library_composition_and_saturation,
     npins.test_per_token_multiplies_by_the_reciprocal,
     npins.test_requant_scales_first_then_the_output_scale,
+    npins.test_per_token_reciprocal_overflow_fixture,
+    lambda: pins.test_nonfinite_amax_fixture(O.FMT_FP32),
+    lambda: pins.test_nonfinite_amax_fixture(O.FMT_UE8M0_PACKED),
     # the slow ones last (several seconds each), so most mutants fail before reaching them
     lambda: pins.test_silu_mul_every_16bit_gate("bf16"),
     pins.test_e4m3_encoder_vs_exhaustive_argmin_and_saturation,

@@ -462,3 +462,22 @@ def test_scale_floor_only_affects_tiny_scales():
     _, a = _run(x, 128, fmt=O.FMT_UE8M0_PACKED)
     _, b = _run(x, 128, fmt=O.FMT_UE8M0_PACKED, flags=O.FLAG_UE8M0_SCALE_FLOOR)
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- infinite amax
+
+@pytest.mark.parametrize("fmt", [O.FMT_FP32, O.FMT_UE8M0_PACKED, O.FMT_UE8M0_FP32])
+def test_nonfinite_amax_fixture(fmt):
+    """Groups whose amax is +inf (an infinite element; a silu product that overflows
+    binary32): the hand-worked codes and scale words of tests/golden/nonfinite_amax.txt,
+    in every scale format and output type."""
+    from golden_fixtures import nonfinite_amax_cases
+    cases = nonfinite_amax_cases()
+    assert len(cases) == 4
+    key = {O.FMT_FP32: "fp32", O.FMT_UE8M0_PACKED: "packed", O.FMT_UE8M0_FP32: "ue8m0_fp32"}[fmt]
+    for c in cases:
+        x = torch.from_numpy(c["x"].view(np.int16).copy()).view(torch.bfloat16).reshape(1, -1)
+        out = O.OUT_E4M3 if c["out"] == "e4m3" else O.OUT_INT8
+        q, s = _run(x, c["group"], out_dtype=out, fmt=fmt, silu=c["silu"])
+        assert np.array_equal(q, c["codes"]), (c["name"], q, c["codes"])
+        assert np.array_equal(s.view(np.uint32), c[key]), (c["name"], s.view(np.uint32), c[key])

@@ -204,3 +204,28 @@ def test_requant_scales_first_then_the_output_scale():
     other = e4m3_bytes(np.clip(v * (xs * inv).astype(np.float32), -448, 448)).reshape(codes.shape)
     assert np.array_equal(out, page)
     assert (other != out).sum() >= 8 * G
+
+
+# ---------------------------------------------------------------- reciprocal overflow
+
+def test_per_token_reciprocal_overflow_fixture():
+    """Rows whose reciprocal 1/s overflows to +inf (max below about 1.3e-36) and one whose
+    s is subnormal with a finite reciprocal: the hand-worked codes of
+    tests/golden/per_token_reciprocal_overflow.txt (the page's clamp, min first, with
+    IEEE minNum / maxNum, so 0 * inf = NaN clamps to +448)."""
+    from golden_fixtures import per_token_overflow_rows
+    rows = per_token_overflow_rows()
+    assert len(rows) == 3
+    for dt, bits, want in rows:
+        H = bits.size
+        q = np.full(H, 0xAB, np.uint8)
+        s = np.full(1, np.nan, np.float32)
+        if dt == "fp32":
+            vals = bits.view(np.float32)
+            O.per_token_quant(vals.reshape(1, H).copy(), O.IN_FP32, q, s)
+        else:
+            vals = (bits.astype(np.uint32) << 16).view(np.float32)
+            O.per_token_quant(bits.reshape(1, H).copy(), O.IN_BF16, q, s)
+        m = np.abs(vals).max().astype(np.float32)
+        assert s[0].view(np.uint32) == (m / F32(448)).astype(np.float32).view(np.uint32)
+        assert np.array_equal(q, want), (dt, q, want)
