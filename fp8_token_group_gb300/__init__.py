@@ -33,7 +33,7 @@ E4M3, INT8 = 0, 1
 SCALE_FP32, SCALE_UE8M0_PACKED, SCALE_UE8M0_FP32 = 0, 1, 2
 ROW_MAJOR, COL_MAJOR_TMA = 0, 1
 FLAG_NO_PDL, FLAG_UE8M0_SCALE_FLOOR, FLAG_FAST_DIVIDE = 1, 2, 4
-EPS_MIN = 1e-24
+EPS_MIN = 2.0 ** -140          # PTGQ_EPS_MIN
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _HEADER = os.path.join(os.path.dirname(_HERE), "include", "ptgq.h")
@@ -131,6 +131,9 @@ def alloc_outputs(x, group_size: int, *, out_dtype: int = E4M3, scale_fmt: int =
     else:
         n, hin = x.shape
         rows = tokens_pad or n
+    if fuse_silu and hin % 2 != 0:
+        raise ValueError(f"fuse_silu needs gate and up halves of equal width; the last "
+                         f"dimension of x is {hin}")
     H = hin // 2 if fuse_silu else hin
     qshape = (n, rows, H) if masked else (rows, H)
     qdt = torch.float8_e4m3fn if out_dtype == E4M3 else torch.int8
@@ -169,6 +172,9 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
             return      # no experts: nothing to read or write (an empty masked_m has no address)
     else:
         n, hin = x.shape
+    if fuse_silu and hin % 2 != 0:
+        raise ValueError(f"fuse_silu needs gate and up halves of equal width; the last "
+                         f"dimension of x is {hin}")
     H = hin // 2 if fuse_silu else hin
     # The library sees raw pointers; check here that the outputs hold what the call writes,
     # so a short buffer is an exception rather than a write past its end.

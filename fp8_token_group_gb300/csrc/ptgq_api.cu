@@ -202,8 +202,12 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   p.eps = eps;
   p.fmax = out_dtype == PTGQ_E4M3 ? 448.0f : 127.0f;
   p.scale_floor = (flags & PTGQ_FLAG_UE8M0_SCALE_FLOOR) ? 1e-10f : 0.0f;
-  p.rows_hint = masked && expected_m > 0
-                    ? static_cast<uint32_t>(std::min<int64_t>(expected_m, g.rows)) : 0u;
+  // Live rows per expert that the prefetch of the first rows guesses: the caller's hint,
+  // or one row per expert without a hint (the first row of an expert is live whenever the
+  // expert has any row, which covers the decode-sized calls where the prefetch matters).
+  p.rows_hint = !masked ? 0u
+                        : static_cast<uint32_t>(std::min<int64_t>(expected_m > 0 ? expected_m : 1,
+                                                                  g.rows));
   p.rows_hint_magic = p.rows_hint <= 1u ? 0xFFFFFFFFu
                                         : static_cast<uint32_t>((uint64_t(1) << 32) / p.rows_hint);
   if (!masked) {
@@ -305,7 +309,7 @@ extern "C" const char* ptgq_strerror(int status) {
     case PTGQ_ERR_ALIGN: return "misaligned pointer (x 32 B, out_q 16 B, out_s and masked_m 4 B)";
     case PTGQ_ERR_SCALE_FMT: return "unknown scale format";
     case PTGQ_ERR_LAYOUT: return "unknown scale layout";
-    case PTGQ_ERR_EPS: return "eps must be finite and >= PTGQ_EPS_MIN (1e-24)";
+    case PTGQ_ERR_EPS: return "eps must be finite and >= PTGQ_EPS_MIN (2^-140)";
     case PTGQ_ERR_FLAG: return "fuse_silu must be 0 or 1 and flags must be PTGQ_FLAG_* bits";
     case PTGQ_ERR_TOO_LARGE: return "sizes exceed the supported index range";
     case PTGQ_ERR_CUDA: return "CUDA launch failed";

@@ -9,13 +9,10 @@ namespace ptgq {
 
 constexpr int kThreads = 256;                 // 8 warps per CTA (all but the fp16 silu instances)
 constexpr int kWarps = kThreads / 32;
-#ifndef PTGQ_TUNE_F16_SILU_THREADS
-#define PTGQ_TUNE_F16_SILU_THREADS 1024
-#endif
 // Threads per CTA of a quantizer instance.  The fp16 fused-silu instances hold a 162 KB
 // table of silu results in shared memory, so one CTA per SM carries all their warps.
 constexpr int quant_threads(bool fp16, bool silu) {
-  return fp16 && silu ? PTGQ_TUNE_F16_SILU_THREADS : kThreads;
+  return fp16 && silu ? 1024 : kThreads;
 }
 // Tasks a CTA of an instance takes in a call too small to fill the grid: one per warp,
 // except in the fp16 silu instances, whose large CTAs then deal consecutive tasks
@@ -58,8 +55,9 @@ struct Params {
   float fmax;                // 448 (e4m3) or 127 (int8)
   float scale_floor;         // UE8M0 only: s = max(s, scale_floor); 1e-10 for the vLLM
                              // semantics, else 0 (a no-op since s > 0)
-  uint32_t rows_hint;        // masked: the caller's expected live rows per expert,
-                             // min(expected_m, rows); 0 without a hint
+  uint32_t rows_hint;        // masked: the live rows per expert that the prefetch of each
+                             // warp's first rows guesses: min(expected_m, rows), or 1
+                             // without a hint; 0 in flat calls
   uint32_t rows_hint_magic;  // floor(2^32 / rows_hint), or 0xFFFFFFFF when rows_hint <= 1
   // Flat zero-fill of padding (rows [T, rows) of q; scale rows past T).
   int64_t zero_q_begin;      // byte offsets into q, multiples of 16

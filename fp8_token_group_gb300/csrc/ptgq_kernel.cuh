@@ -34,6 +34,21 @@ namespace ptgq {
 
 constexpr int kSiluF16Words = (PTGQ_SILU_F16_ENTRIES + 3) / 4 * 4;
 constexpr int kSiluBf16Words = 2 * PTGQ_SILU_BF16_SPAN;
+// Range of amax over which the fast scale and quotient arithmetic is proven exact (checked
+// for every pair of 16-bit values and 1.3e9 sampled binary32 pairs down to this amax).
+constexpr float kExactAmaxMin = 1e-24f;
+constexpr float kFltMax = 3.40282346638528859812e+38f;
+
+// IEEE quotient v / scale for the warps outside that range, made ready for the code
+// conversion: a NaN quotient (inf / inf, an infinite element of a group whose amax is
+// infinite) becomes the positive NaN, which the saturating e4m3 conversion encodes 0x7F,
+// or 0 for int8 (NaN has no integer value).
+template <bool kInt8>
+__device__ __forceinline__ float exact_quotient(float v, float scale) {
+  const float y = __fdiv_rn(v, scale);
+  if (y == y) return y;
+  return kInt8 ? 0.0f : __uint_as_float(0x7FFFFFFFu);
+}
 
 template <bool kFp16, bool kSilu>
 struct SmemTables {
@@ -55,18 +70,7 @@ struct Slot {
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
 // CTAs/SM (64 registers).  bf16 silu, 3 CTAs/SM: flat one task pipelined, masked two tasks
 // loaded then computed.  fp16 silu: one CTA of quant_threads() per SM (its table fills most
-// of the shared memory), one task pipelined.  PTGQ_TUNE_BATCH / _SILU_BATCH / _PIPELINE /
-// _MIN_BLOCKS override all bf16-silu and plain instances, PTGQ_TUNE_F16_SILU_BATCH /
-// _PIPELINE the fp16 silu ones (sweeps).
-#ifndef PTGQ_TUNE_SILU_BATCH
-#define PTGQ_TUNE_SILU_BATCH 1
-#endif
-#ifndef PTGQ_TUNE_F16_SILU_BATCH
-#define PTGQ_TUNE_F16_SILU_BATCH 1
-#endif
-#ifndef PTGQ_TUNE_F16_SILU_PIPELINE
-#define PTGQ_TUNE_F16_SILU_PIPELINE 1
-#endif
+// of the shared memory), one task pipelined.
 // The light flavour of the plain flat instances (kLight): one task per batch at 6 CTAs/SM
 // (40 registers, 48 warps per SM).  It ramps up faster when each warp has only a few
 // tasks, and the launcher takes it below about 8 tasks per warp of the standard grid
@@ -83,17 +87,9 @@ struct Tuning {
   // against 15.2 us round-robin for fp16 silu [8192, 2x2048]; masked silu [32, 384,
   // 2x4096]: 22.9 us round-robin against 23.3 us.)
   static constexpr bool round_robin = f16_silu;
-#ifdef PTGQ_TUNE_BATCH
-  static constexpr int batch = f16_silu ? PTGQ_TUNE_F16_SILU_BATCH
-                                        : (kSilu ? PTGQ_TUNE_SILU_BATCH : PTGQ_TUNE_BATCH);
-  static constexpr bool pipeline = f16_silu ? PTGQ_TUNE_F16_SILU_PIPELINE : PTGQ_TUNE_PIPELINE;
-  static constexpr int min_blocks = f16_silu ? 1 : PTGQ_TUNE_MIN_BLOCKS;
-#else
-  static constexpr int batch =
-      f16_silu ? PTGQ_TUNE_F16_SILU_BATCH : ((kLight || (kSilu && !kMasked)) ? 1 : 2);
-  static constexpr bool pipeline = f16_silu ? PTGQ_TUNE_F16_SILU_PIPELINE : (kSilu && !kMasked);
+  static constexpr int batch = (f16_silu || kLight || (kSilu && !kMasked)) ? 1 : 2;
+  static constexpr bool pipeline = f16_silu || (kSilu && !kMasked);
   static constexpr int min_blocks = f16_silu ? 1 : (kLight ? 6 : (!kSilu ? 4 : 3));
-#endif
 };
 
 // kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32, 3 fp32 scales with
@@ -131,8 +127,8 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   int32_t* bucket = prefix + (p.n + 1);
   uint32_t bshift = 0u;
   if constexpr (kMasked) {
-    // With a hint of the live rows per expert, the rows of this warp's first task, guessed
-    // as if every expert had exactly rows_hint live rows, go to L2 while masked_m is read
+    // The rows of this warp's first task, guessed as if every expert had exactly rows_hint
+    // live rows (the caller's expected_m, else one), go to L2 while masked_m is read
     // (hinted decode batch, bf16 silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us).
     // The guess only decides what is prefetched: rows below rows_hint <= rows of experts
     // below n, so every prefetched address lies inside x.
@@ -302,28 +298,51 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
     }
     amax_bits = group_max(sl.valid ? amax_bits : 0u, lg);
     const float amax = fmaxf(u2f(amax_bits), p.eps);
-    float s = div_by_const(amax, p.fmax, rfmax);
+    float s;
     uint32_t e = 0u;
     uint64_t y[8];
-    if constexpr (kPow2) {
-      s = fmaxf(s, p.scale_floor);
-      e = ue8m0_exponent(s);
-      const float inv = ue8m0_inverse(e);
-      const uint64_t inv2 = pk2(inv, inv);
+    // The scale and quotients below (constant reciprocal with one correction, reciprocal
+    // with an exact residual) give the IEEE results for kExactAmaxMin <= amax <= FLT_MAX.
+    // A warp with any group outside that range -- a tiny eps over an all-zero group, tiny
+    // data, or an infinite amax from an infinite element or a silu product that overflows
+    // binary32 -- takes IEEE division for the scale and every quotient instead (uniform
+    // branch; real activations never reach it).
+    if (__all_sync(0xFFFFFFFFu, amax >= kExactAmaxMin && amax <= kFltMax)) {
+      s = div_by_const(amax, p.fmax, rfmax);
+      if constexpr (kPow2) {
+        s = fmaxf(s, p.scale_floor);
+        e = ue8m0_exponent(s);
+        const float inv = ue8m0_inverse(e);
+        const uint64_t inv2 = pk2(inv, inv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = mul2(v[i], inv2);
-    } else if constexpr (kFmt == 3) {
+        for (int i = 0; i < 8; ++i) y[i] = mul2(v[i], inv2);
+      } else if constexpr (kFmt == 3) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float v0, v1;
+          upk2(v[i], v0, v1);
+          y[i] = pk2(__fdividef(v0, s), __fdividef(v1, s));
+        }
+      } else {
+        const float r = __frcp_rn(s);
+        const uint64_t r2 = pk2(r, r), ns2 = pk2(-s, -s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = div2_by_scale(v[i], r2, ns2);
+      }
+    } else {
+      s = __fdiv_rn(amax, p.fmax);
+      float scale = s;
+      if constexpr (kPow2) {
+        s = fmaxf(s, p.scale_floor);
+        e = ue8m0_exponent(s);
+        scale = u2f(e << 23);        // 2^(e - 127): e >= 1 since s > 0; +inf for e = 255
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float v0, v1;
         upk2(v[i], v0, v1);
-        y[i] = pk2(__fdividef(v0, s), __fdividef(v1, s));
+        y[i] = pk2(exact_quotient<kInt8>(v0, scale), exact_quotient<kInt8>(v1, scale));
       }
-    } else {
-      const float r = __frcp_rn(s);
-      const uint64_t r2 = pk2(r, r), ns2 = pk2(-s, -s);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = div2_by_scale(v[i], r2, ns2);
     }
     uint32_t o[4];
     if constexpr (kInt8) {

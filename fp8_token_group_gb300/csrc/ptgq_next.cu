@@ -10,7 +10,7 @@
 //    below masked_m[e]; other rows are not touched.
 //
 // Both are streaming kernels bound by HBM bandwidth: persistent grids, full-width
-// vector loads and stores, PDL, no shared-memory staging beyond the masked prefix.
+// vector loads and stores, PDL.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -80,6 +80,31 @@ __device__ __forceinline__ void quantize16(const uint32_t (&w)[4], float inv, ui
   }
 }
 
+// The same for a row whose reciprocal scale or scale is infinite (a row maximum below about
+// 1.3e-36, where 1/s overflows, or an infinite element): the products, which can be NaN
+// (0 * inf) or infinite there, go through the page's clamp, max(min(y, 448), -448) with
+// IEEE minNum / maxNum (NaN yields the other operand), before the conversion.
+template <int kIn>
+__device__ __forceinline__ void quantize16_clamped(const uint32_t (&w)[4], float inv, uint8_t* dst) {
+  auto q = [&](float xv) { return fmaxf(fminf(__fmul_rn(xv, inv), 448.0f), -448.0f); };
+  if constexpr (kIn == 2) {
+    const uint32_t o = e4m3x4(q(u2f(w[0])), q(u2f(w[1])), q(u2f(w[2])), q(u2f(w[3])));
+    asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(o) : "memory");
+  } else {
+    constexpr bool h = kIn == 1;
+    const uint32_t o0 = e4m3x4(q(widen_lo<h>(w[0])), q(widen_hi<h>(w[0])), q(widen_lo<h>(w[1])),
+                               q(widen_hi<h>(w[1])));
+    const uint32_t o1 = e4m3x4(q(widen_lo<h>(w[2])), q(widen_hi<h>(w[2])), q(widen_lo<h>(w[3])),
+                               q(widen_hi<h>(w[3])));
+    asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(dst), "r"(o0), "r"(o1) : "memory");
+  }
+}
+
+// Whether a row takes quantize16_clamped (uniform over the warp that owns the row).
+__device__ __forceinline__ bool row_needs_clamp(float s, float inv) {
+  return fabsf(inv) == INFINITY || fabsf(s) == INFINITY;
+}
+
 // Rows staged in shared memory.  A warp owns one row at a time and kPtBufs row buffers:
 // 2 when it takes several rows (the copy of its next row, cp.async with 16 bytes per lane
 // per instruction, is in flight while it reduces and quantizes the current one), 1 when
@@ -135,10 +160,18 @@ __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerToken
     const float s = __fdiv_rn(u2f(m), 448.0f);
     const float inv = s == 0.0f ? 0.0f : __frcp_rn(s);
     uint8_t* qrow = p.q + row * p.hidden;
-    for (int64_t c = lane; c < chunks; c += 32) {
-      uint32_t w[4];
-      chunk(slot, c, w);
-      quantize16<kIn>(w, inv, qrow + c * kPer16);
+    if (!row_needs_clamp(s, inv)) {
+      for (int64_t c = lane; c < chunks; c += 32) {
+        uint32_t w[4];
+        chunk(slot, c, w);
+        quantize16<kIn>(w, inv, qrow + c * kPer16);
+      }
+    } else {
+      for (int64_t c = lane; c < chunks; c += 32) {
+        uint32_t w[4];
+        chunk(slot, c, w);
+        quantize16_clamped<kIn>(w, inv, qrow + c * kPer16);
+      }
     }
     if (lane == 0) p.s[row] = s;
     issue(row + kPtBufs * W, slot);                        // refill this buffer
@@ -172,14 +205,21 @@ __global__ void __launch_bounds__(kThreads) per_token_reg_kernel(const PerTokenP
       asm volatile("ld.global.nc.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(ptr));
     }
   };
-  auto quantize_store = [&](int64_t row, int64_t i, const uint32_t (&w)[kWords], float inv) {
+  // clamp: the row takes the page's clamp before the conversion (row_needs_clamp)
+  auto quantize_store = [&](int64_t row, int64_t i, const uint32_t (&w)[kWords], float inv,
+                            bool clamp) {
     uint8_t* dst = p.q + row * p.hidden + i * kElems;
     if constexpr (kVecBytes == 16) {
-      quantize16<kIn>(w, inv, dst);
+      if (clamp) quantize16_clamped<kIn>(w, inv, dst);
+      else quantize16<kIn>(w, inv, dst);
     } else {       // 16-bit, 4 elements
       constexpr bool h = kIn == 1;
-      const uint32_t o = e4m3x4(__fmul_rn(widen_lo<h>(w[0]), inv), __fmul_rn(widen_hi<h>(w[0]), inv),
-                                __fmul_rn(widen_lo<h>(w[1]), inv), __fmul_rn(widen_hi<h>(w[1]), inv));
+      auto q = [&](float xv) {
+        const float y = __fmul_rn(xv, inv);
+        return clamp ? fmaxf(fminf(y, 448.0f), -448.0f) : y;
+      };
+      const uint32_t o = e4m3x4(q(widen_lo<h>(w[0])), q(widen_hi<h>(w[0])), q(widen_lo<h>(w[1])),
+                                q(widen_hi<h>(w[1])));
       asm volatile("st.global.b32 [%0], %1;" ::"l"(dst), "r"(o) : "memory");
     }
   };
@@ -204,15 +244,16 @@ __global__ void __launch_bounds__(kThreads) per_token_reg_kernel(const PerTokenP
     m = redux_max(abs_bits<kIn>(m), 0xFFFFFFFFu);
     const float s = __fdiv_rn(u2f(m), 448.0f);
     const float inv = s == 0.0f ? 0.0f : __frcp_rn(s);
+    const bool clamp = row_needs_clamp(s, inv);
 #pragma unroll
     for (int j = 0; j < kCache; ++j) {
       const int64_t i = lane + 32 * j;
-      if (i < nvec) quantize_store(row, i, cache[j], inv);
+      if (i < nvec) quantize_store(row, i, cache[j], inv, clamp);
     }
     for (int64_t i = lane + 32 * kCache; i < nvec; i += 32) {
       uint32_t w[kWords];
       load(row, i, w);
-      quantize_store(row, i, w, inv);
+      quantize_store(row, i, w, inv, clamp);
     }
     if (lane == 0) p.s[row] = s;
   }
@@ -226,70 +267,146 @@ struct RequantParams {
   const int32_t* masked_m;       // nullptr: every row is live
   const float* output_scale;     // device scalar
   uint8_t* out;
-  int64_t experts;
-  int64_t m;                     // rows per expert
-  int64_t k;                     // row length
+  uint32_t experts;              // E
+  uint32_t m;                    // rows per expert
+  int64_t k;                     // row length (codes)
   int64_t se, sm, sg;            // x_scale strides (elements)
-  uint32_t lg_log2;              // log2(lanes per group) = log2(G / 16)
-  uint32_t gpr;                  // groups per row
-  uint32_t gpr_magic;            // floor(2^32 / gpr), or 0xFFFFFFFF when gpr == 1
+  uint32_t cpr;                  // lane chunks per row: k / kV
+  uint32_t cpr_magic;            // floor(2^32 / cpr), or 0xFFFFFFFF when cpr == 1
+  uint32_t e_magic;              // floor(2^32 / E), or 0xFFFFFFFF when E == 1
+  uint32_t g_log2;               // log2(group size)
 };
 
-// Each lane requantizes 16 codes (16 bytes) of one group; G/16 lanes share a group's scale.
-__global__ void __launch_bounds__(kThreads) requant_kernel(const RequantParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  int32_t* prefix = reinterpret_cast<int32_t*>(smem);
+constexpr int kRequantBlocksPerSm = 4;
+
+// Requantizes kV codes (kV = 32, or 16 when k is not a multiple of 32) of one row per lane.
+//
+// Row slots are numbered row-major over (row, expert): slot S = r * E + e, so the rows most
+// likely to be live -- the first rows of every expert -- come first, and every live row lies
+// below max_e masked_m[e] * E slots.  A warp task is 32 consecutive lane chunks of that
+// numbering (a row of expert e is contiguous in x, so a task is at most a few contiguous
+// runs).  Each warp reads masked_m itself (one word per lane for E <= 32) and takes the
+// maximum with redux.sync, which bounds its task loop; a lane then knows whether its chunk
+// is live from masked_m[e] (a shuffle for E <= 32, else an L1-cached load).  Dead chunks
+// are neither read nor written.  So the only dependent round trip before the row loads is
+// the read of masked_m: no prefix sum, no block barrier, no search for the expert.
+// Batches of two tasks are loaded, then computed, when a warp has more than one task.
+template <int kV>
+__global__ void __launch_bounds__(kThreads, kRequantBlocksPerSm) requant_kernel(const RequantParams p) {
+  constexpr int kWords = kV / 4;
   griddep_wait();
   griddep_launch_dependents();
-  const float oscale = *p.output_scale;                 // in flight during the prefix sum
-  const bool masked = p.masked_m != nullptr;
-  uint32_t live_rows = static_cast<uint32_t>(p.experts * p.m);
-  if (masked) masked_prefix(p.masked_m, p.experts, p.m, prefix);
-  __syncthreads();
-  if (masked) live_rows = static_cast<uint32_t>(prefix[p.experts]);
-  const float inv = __frcp_rn(oscale);
-
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t lg = 1u << p.lg_log2;
-  const uint32_t kk = lane & (lg - 1u);
-  const uint32_t gpw_log2 = 5u - p.lg_log2;                 // groups per warp task
-  const uint32_t total_groups = live_rows * p.gpr;
-  const uint32_t tasks = (total_groups + (1u << gpw_log2) - 1u) >> gpw_log2;
+  const float oscale = *p.output_scale;                 // in flight with masked_m
+  const bool masked = p.masked_m != nullptr;
+  // Live rows of expert `lane` (E <= 32), and the largest live count of any expert.
+  uint32_t my_live = 0u, max_live = p.m;
+  if (masked) {
+    uint32_t mx = 0u;
+    for (uint32_t e = lane; e < p.experts; e += 32u) {
+      const int32_t v = p.masked_m[e];
+      const uint32_t c = v < 0 ? 0u : min(static_cast<uint32_t>(v), p.m);
+      if (e == lane) my_live = c;
+      mx = max(mx, c);
+    }
+    max_live = redux_max(mx, 0xFFFFFFFFu);
+  }
+  const float inv = __frcp_rn(oscale);
+  const uint64_t inv2 = pk2(inv, inv);
+
+  // Tasks that can hold live chunks: those of the first max_live * E slots.
+  const uint64_t live_chunks = static_cast<uint64_t>(max_live) * p.experts * p.cpr;
+  const uint32_t tasks = static_cast<uint32_t>((live_chunks + 31u) >> 5);
+  const uint32_t warp_id = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const uint32_t stride = gridDim.x * kWarps;
-  for (uint32_t t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < tasks; t += stride) {
-    const uint32_t gi = (t << gpw_log2) + (lane >> p.lg_log2);
-    if (gi >= total_groups) continue;
-    const uint32_t R = udiv(gi, p.gpr, p.gpr_magic);
-    const uint32_t g = gi - R * p.gpr;
-    int64_t e = 0, r = R;
+
+  struct Chunk {
+    int64_t off;           // byte offset of the chunk in x and out
+    float sc0, sc1;        // group scale(s): two when a chunk spans two groups (G = 16, kV = 32)
+    bool live;
+    uint32_t w[kWords];
+  };
+
+  auto issue = [&](uint32_t t, Chunk& ch) {
+    const uint32_t c = (t << 5) + lane;
+    const uint32_t S = udiv(c, p.cpr, p.cpr_magic);
+    const uint32_t col = c - S * p.cpr;
+    const uint32_t r = udiv(S, p.experts, p.e_magic);
+    const uint32_t e = S - r * p.experts;
+    uint32_t live_e = p.m;
     if (masked) {
-      e = expert_of(prefix, static_cast<int>(p.experts), R);
-      r = R - prefix[e];
-    } else {
-      e = R / p.m;
-      r = R - e * p.m;
-    }
-    const int64_t off = (e * p.m + r) * p.k + (static_cast<int64_t>(g) << (p.lg_log2 + 4)) + kk * 16;
-    uint32_t w[4];
-    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p.x + off));
-    const float sc = p.x_scale[e * p.se + r * p.sm + static_cast<int64_t>(g) * p.sg];
-    // (v * sc) * inv two codes at a time: mul.rn.f32x2 rounds each product like __fmul_rn
-    const uint64_t sc2 = pk2(sc, sc), inv2 = pk2(inv, inv);
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t c[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t f16x2;
-        const uint16_t pair = static_cast<uint16_t>(w[i] >> (16 * h));
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
-        c[h] = e4m3x2_pair(mul2(mul2(widen2<true>(f16x2), sc2), inv2));
+      if (p.experts <= 32u) {
+        live_e = __shfl_sync(0xFFFFFFFFu, my_live, e & 31u);
+      } else {
+        const int32_t v = __ldg(p.masked_m + e);
+        live_e = v < 0 ? 0u : min(static_cast<uint32_t>(v), p.m);
       }
-      o[i] = c[0] | (c[1] << 16);
     }
-    st_128(p.out + off, o[0], o[1], o[2], o[3]);
+    ch.live = static_cast<uint64_t>(c) < live_chunks && r < live_e;
+    ch.off = (static_cast<int64_t>(e) * p.m + r) * p.k + static_cast<int64_t>(col) * kV;
+    if (ch.live) {
+      const uint8_t* src = p.x + ch.off;
+      if constexpr (kV == 32) {
+        asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(ch.w[0]), "=r"(ch.w[1]), "=r"(ch.w[2]), "=r"(ch.w[3]), "=r"(ch.w[4]),
+                       "=r"(ch.w[5]), "=r"(ch.w[6]), "=r"(ch.w[7])
+                     : "l"(src));
+      } else {
+        asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(ch.w[0]), "=r"(ch.w[1]), "=r"(ch.w[2]), "=r"(ch.w[3]) : "l"(src));
+      }
+      const uint32_t g = static_cast<uint32_t>((static_cast<uint64_t>(col) * kV) >> p.g_log2);
+      const float* sp = p.x_scale + static_cast<int64_t>(e) * p.se + static_cast<int64_t>(r) * p.sm;
+      ch.sc0 = __ldg(sp + static_cast<int64_t>(g) * p.sg);
+      ch.sc1 = ch.sc0;
+      if (kV == 32 && p.g_log2 == 4u) ch.sc1 = __ldg(sp + static_cast<int64_t>(g + 1u) * p.sg);
+    }
+  };
+
+  // (v * sc) * inv for 4 codes of one 32-bit word, two at a time (mul.rn.f32x2 rounds
+  // each product like __fmul_rn), re-encoded with the saturating conversion.
+  auto word = [&](uint32_t w, float sc) {
+    const uint64_t sc2 = pk2(sc, sc);
+    uint32_t c[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t f16x2;
+      const uint16_t pair = static_cast<uint16_t>(w >> (16 * h));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+      c[h] = e4m3x2_pair(mul2(mul2(widen2<true>(f16x2), sc2), inv2));
+    }
+    return c[0] | (c[1] << 16);
+  };
+
+  auto finish = [&](const Chunk& ch) {
+    if (!ch.live) return;
+    uint32_t o[kWords];
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) o[i] = word(ch.w[i], i < kWords / 2 ? ch.sc0 : ch.sc1);
+    uint8_t* dst = p.out + ch.off;
+    if constexpr (kV == 32) {
+      asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(o[0]),
+                   "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                   : "memory");
+    } else {
+      st_128(dst, o[0], o[1], o[2], o[3]);
+    }
+  };
+
+  uint32_t t = warp_id;
+  if (t + stride < tasks) {                // at least two tasks: batches of two
+    for (; t + stride < tasks; t += 2u * stride) {
+      Chunk a, b;
+      issue(t, a);
+      issue(t + stride, b);
+      finish(a);
+      finish(b);
+    }
+  }
+  if (t < tasks) {
+    Chunk a;
+    issue(t, a);
+    finish(a);
   }
 }
 
@@ -492,8 +609,12 @@ extern "C" int ptgq_requant_per_tensor(const void* x, const float* x_scale, int6
   if (k <= 0 || k % group_size != 0) return PTGQ_ERR_HIDDEN;
   if (num_experts < 0 || m < 0 || (masked_m != nullptr && num_experts > kMaxExperts))
     return PTGQ_ERR_SHAPE;
-  if (num_experts > 0 && m > 0 &&
-      (num_experts * m > (int64_t(1) << 31) / (k / group_size) || m > (int64_t(1) << 31)))
+  // Lane chunks (16 codes at least) are numbered in 32 bits on the device: each factor is
+  // bounded on its own before the product is formed, so nothing overflows.
+  const int64_t kLimit = int64_t(1) << 31;
+  if (num_experts >= kLimit || m >= kLimit || k >= (int64_t(1) << 40) ||
+      (num_experts > 0 && m > kLimit / num_experts) ||
+      (num_experts * m > 0 && k / 16 > (kLimit - 1) / (num_experts * m)))
     return PTGQ_ERR_TOO_LARGE;
   if (num_experts * m == 0) return PTGQ_OK;
   if (x == nullptr || x_scale == nullptr || output_scale == nullptr || out == nullptr)
@@ -502,27 +623,31 @@ extern "C" int ptgq_requant_per_tensor(const void* x, const float* x_scale, int6
       reinterpret_cast<uintptr_t>(x_scale) % 4 != 0 || reinterpret_cast<uintptr_t>(output_scale) % 4 != 0 ||
       reinterpret_cast<uintptr_t>(masked_m) % 4 != 0)
     return PTGQ_ERR_ALIGN;
+  // 32 codes per lane when every row start is 32-byte aligned, else 16.
+  const bool wide = k % 32 == 0 && reinterpret_cast<uintptr_t>(x) % 32 == 0 &&
+                    reinterpret_cast<uintptr_t>(out) % 32 == 0;
+  const int V = wide ? 32 : 16;
   RequantParams p{};
   p.x = static_cast<const uint8_t*>(x);
   p.x_scale = x_scale;
   p.masked_m = masked_m;
   p.output_scale = output_scale;
   p.out = static_cast<uint8_t*>(out);
-  p.experts = num_experts;
-  p.m = m;
+  p.experts = static_cast<uint32_t>(num_experts);
+  p.m = static_cast<uint32_t>(m);
   p.k = k;
   p.se = scale_stride_e;
   p.sm = scale_stride_m;
   p.sg = scale_stride_g;
-  p.lg_log2 = static_cast<uint32_t>(__builtin_ctz(static_cast<unsigned>(group_size / 16)));
-  p.gpr = static_cast<uint32_t>(k / group_size);
-  p.gpr_magic = p.gpr == 1 ? 0xFFFFFFFFu : static_cast<uint32_t>((uint64_t(1) << 32) / p.gpr);
-  const size_t smem = masked_m ? static_cast<size_t>(num_experts + 1) * sizeof(int32_t) : 0;
-  const void* fn = reinterpret_cast<const void*>(&requant_kernel);
-  const int64_t groups = num_experts * m * (k / group_size);
-  const int64_t tasks = (groups * (group_size / 16) + 31) / 32;
-  const int grid = grid_for(fn, smem, (tasks + kWarps - 1) / kWarps);
+  p.cpr = static_cast<uint32_t>(k / V);
+  p.cpr_magic = p.cpr == 1 ? 0xFFFFFFFFu : static_cast<uint32_t>((uint64_t(1) << 32) / p.cpr);
+  p.e_magic = p.experts == 1 ? 0xFFFFFFFFu : static_cast<uint32_t>((uint64_t(1) << 32) / p.experts);
+  p.g_log2 = static_cast<uint32_t>(__builtin_ctz(static_cast<unsigned>(group_size)));
+  const void* fn = wide ? reinterpret_cast<const void*>(&requant_kernel<32>)
+                        : reinterpret_cast<const void*>(&requant_kernel<16>);
+  const int64_t tasks = (num_experts * m * p.cpr + 31) / 32;
+  const int grid = grid_for(fn, 0, (tasks + kWarps - 1) / kWarps);
   if (grid < 0) return PTGQ_ERR_CUDA;
   void* args[] = {&p};
-  return launch(fn, grid, smem, stream, args);
+  return launch(fn, grid, 0, stream, args);
 }

@@ -83,16 +83,17 @@ enum {
   PTGQ_ERR_ALIGN = -7,      /* x not 32-byte, out_q not 16-byte or out_s not 4-byte aligned */
   PTGQ_ERR_SCALE_FMT = -8,  /* unknown scale format */
   PTGQ_ERR_LAYOUT = -9,     /* unknown scale layout */
-  PTGQ_ERR_EPS = -10,       /* eps not finite or below PTGQ_EPS_MIN */
+  PTGQ_ERR_EPS = -10,       /* eps not finite or below PTGQ_EPS_MIN (2^-140) */
   PTGQ_ERR_FLAG = -11,      /* fuse_silu not 0 or 1, or an unknown flag bit */
   PTGQ_ERR_TOO_LARGE = -12, /* more than 2^31 - 1 work units (live rows times groups, or
                              * times packed words, per row), or an index beyond 2^62 */
   PTGQ_ERR_CUDA = -13       /* the kernel launch failed */
 };
 
-/* Smallest accepted eps.  Down to this floor the kernel's division by the scale is proven
- * to give the same codes as IEEE division for every input. */
-#define PTGQ_EPS_MIN 1e-24f
+/* Smallest accepted eps, 2^-140.  It keeps the scale of an all-zero group positive:
+ * RN(eps / FMAX) is at least the smallest binary32 subnormal for every eps >= 2^-140, while
+ * a smaller eps could round it to zero and leave the group without a scale. */
+#define PTGQ_EPS_MIN 0x1p-140f
 
 /*
  * ptgq_quant -- per-token-group quantization, flat or masked (EP-MoE) scheduler.
@@ -124,6 +125,12 @@ enum {
  *   eps             floor of amax; finite and >= PTGQ_EPS_MIN.
  *   stream          CUDA stream of the launch.
  * Returns PTGQ_OK or a negative status.
+ *
+ * Non-finite amax.  x is finite in normal use, but a silu product can overflow binary32
+ * to +-inf (and x may hold an infinity).  Such a group follows the same definition:
+ * amax = +inf, s = +inf (fp32 format), e = 255 (UE8M0: byte 0xFF; float scale +inf).  Each
+ * quotient v / +inf is a signed zero for finite v (codes 0x00 / 0x80, int8 0) and NaN for
+ * an infinite v, encoded 0x7F (the e4m3 NaN) or 0 (int8).  Other groups are unaffected.
  */
 int ptgq_quant(const void* x, int dtype, int64_t num_tokens_or_E, int64_t tokens_pad,
                int64_t hidden, int group_size, void* out_q, int out_dtype, void* out_s,
@@ -156,9 +163,9 @@ enum {
  *               the grid is sized for every row of tokens_pad being live; with one it is
  *               sized for E * min(expected_m, tokens_pad) rows.  Results are the same for
  *               any value: the grid strides over whatever rows are live, so a low hint
- *               costs time, never correctness.  With a hint, rows below
- *               min(expected_m, tokens_pad) of x may be prefetched into L2 before the
- *               live counts are known (a cache hint: their contents never reach the
+ *               costs time, never correctness.  Rows below min(expected_m, tokens_pad)
+ *               of x (below 1 without a hint) may be prefetched into L2 before the live
+ *               counts are known (a cache hint: their contents never reach the
  *               outputs), so x must span its whole [E, tokens_pad, H_in] extent, as
  *               ptgq_quant requires.  0: no hint.  Ignored in flat mode.
  *               Negative: PTGQ_ERR_SHAPE. */

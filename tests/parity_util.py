@@ -14,9 +14,10 @@ from fp8_token_group_gb300 import synth
 
 GUARD = 4096          # bytes of canary before and after each output buffer
 CANARY = 0xA5
-# Sentinels no kernel output can equal: e4m3 0x7F is NaN (satfinite never emits it),
-# int8 0x80 = -128 is unreachable (|y| <= 127), float scale 0x7FC00001 is a NaN, and a
-# packed word of 0xFFFFFFFF holds exponent byte 255, which finite inputs never give.
+# Sentinels no kernel output can equal in rows the kernel must leave alone: e4m3 0x7F is
+# NaN (emitted only for an infinite element of a group whose amax is infinite), int8 0x80
+# = -128 is unreachable (|y| <= 127), float scale 0x7FC00001 is a NaN payload no scale
+# has, and a packed word of 0xFFFFFFFF holds exponent byte 255 in all four bytes.
 SENT_Q = {P.E4M3: 0x7F, P.INT8: 0x80}
 SENT_S_FLOAT = 0x7FC00001
 SENT_S_PACKED = 0xFFFFFFFF

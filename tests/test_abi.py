@@ -43,6 +43,15 @@ def test_header_constants_match_binding():
                                               P.FLAG_FAST_DIVIDE)
 
 
+def test_eps_floor_matches_binding_and_keeps_the_scale_positive():
+    text = open(HEADER).read()
+    m = re.search(r"#define PTGQ_EPS_MIN (\S+)", text).group(1)
+    assert float.fromhex(m.rstrip("f")) == P.EPS_MIN == 2.0 ** -140
+    import numpy as np
+    for fmax in (448, 127):
+        assert np.float32(P.EPS_MIN) / np.float32(fmax) > 0
+
+
 def test_strerror_covers_every_status(L):
     for code in range(-13, 1):
         msg = P.strerror(code)
@@ -84,7 +93,7 @@ def test_validation_codes(L):
     assert _call(L, s=2) == -7
     assert _call(L, fmt=3) == -8
     assert _call(L, layout=2) == -9
-    for eps in (0.0, -1.0, 1e-30, float("inf"), float("nan")):
+    for eps in (0.0, -1.0, 2.0 ** -141, 1e-45, float("inf"), float("nan")):
         assert _call(L, eps=eps) == -10
     assert _call(L, silu=2) == -11
     assert _call(L, flags=8) == -11

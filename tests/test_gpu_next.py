@@ -117,3 +117,70 @@ def test_per_token_row_sizes_in_any_order():
         x = synth.sweep_input(hidden, 64, hidden, torch.float32)
         gq, gs, oq, os_ = _per_token_both(x, 64)
         assert np.array_equal(gq, oq) and np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+
+
+def test_per_token_reciprocal_overflow_fixture_and_tiny_rows():
+    """Rows whose reciprocal scale overflows (max below about 1.3e-36) take the page's clamp
+    (0 * inf = NaN clamps to +448); the hand-worked fixture rows, then random tiny rows of
+    every dtype through the staged kernel (hidden 512) and the register kernel (hidden 4,
+    1076), mixed with ordinary rows in the same call."""
+    from golden_fixtures import per_token_overflow_rows
+    for dt, bits, want in per_token_overflow_rows():
+        if dt == "fp32":
+            x = torch.from_numpy(bits.view(np.float32).copy()).reshape(1, -1)
+        else:
+            x = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(1, -1)
+        # the fixture row, tiled to a 16-byte multiple so both kernels can take it
+        xx = x.repeat(1, 8)
+        gq, gs, oq, os_ = _per_token_both(xx, 1)
+        assert np.array_equal(oq[: want.size], want)
+        assert np.array_equal(gq, oq) and np.array_equal(gs.view(np.uint32), os_.view(np.uint32))
+    g = torch.Generator().manual_seed(9)
+    for dt in (torch.float32, torch.bfloat16):
+        for hidden in (4, 512, 1076):
+            x = torch.randn((24, hidden), generator=g)
+            tiny = torch.tensor([1e-37, 2.0 ** -133, 1.5e-36, 3e-39, 1e-36, 1e-38])
+            for i in range(12):
+                x[2 * i] *= tiny[i % tiny.numel()]
+            x[1::6] = 0
+            x[3, : hidden // 2] = 0
+            x[4, 0] = 0
+            x = x.to(dt)
+            gq, gs, oq, os_ = _per_token_both(x, 24)
+            assert np.array_equal(gq, oq), (dt, hidden)
+            assert np.array_equal(gs.view(np.uint32), os_.view(np.uint32)), (dt, hidden)
+
+
+def test_requant_chunk_widths_many_experts_and_unaligned_views():
+    """32 codes per lane (rows a multiple of 32 codes, 32-byte aligned) and 16 (k = 16 * odd,
+    or x / out views offset by 16 bytes); more than 32 experts (live counts read per lane
+    instead of shuffled); out-of-range live counts; no masked_m."""
+    g = torch.Generator().manual_seed(3)
+    for E, M, K, group, off in [(3, 40, 1040, 16, 0), (40, 12, 512, 64, 0), (5, 33, 1024, 16, 0),
+                                (4, 20, 2048, 128, 16), (2, 7, 96, 32, 16)]:
+        codes = torch.randint(0, 256, (E, M, K), generator=g, dtype=torch.uint8).numpy()
+        codes[(codes & 0x7F) == 0x7F] = 0
+        xs = (torch.rand((E, M, K // group), generator=g) * 4 + 1e-3).numpy().astype(np.float32)
+        masked = torch.randint(-3, M + 4, (E,), generator=g, dtype=torch.int32).numpy()
+        masked[0] = M
+        strides = (M * (K // group), K // group, 1)
+        if off == 0:
+            for mm in (masked, None):
+                got, ref = _requant_both(codes, xs, strides, mm, 0.37, group)
+                assert np.array_equal(got, ref), (E, M, K, group)
+            continue
+        # x and out as views 16 bytes into larger buffers
+        xbig = torch.zeros(E * M * K + 64, dtype=torch.uint8, device="cuda")
+        xv = xbig[off:off + E * M * K].view(E, M, K)
+        xv.copy_(torch.from_numpy(codes))
+        obig = torch.full((E * M * K + 64,), 0x2C, dtype=torch.uint8, device="cuda")
+        ov = obig[off:off + E * M * K].view(E, M, K)
+        sd = torch.as_strided(torch.from_numpy(xs.ravel().copy()).cuda(), (E, M, K // group), strides)
+        osc = torch.tensor([0.37], dtype=torch.float32, device="cuda")
+        P.requant_per_tensor(xv, sd, torch.from_numpy(masked).cuda(), osc, ov, group_size=group)
+        torch.cuda.synchronize()
+        ref = np.full((E, M, K), 0x2C, np.uint8)
+        O.requant_per_tensor(codes, xs.ravel().copy(), strides, masked, 0.37, ref, group)
+        ob = obig.cpu().numpy()
+        assert np.array_equal(ob[off:off + E * M * K].reshape(E, M, K), ref)
+        assert np.all(ob[:off] == 0x2C) and np.all(ob[off + E * M * K:] == 0x2C)

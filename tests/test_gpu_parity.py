@@ -269,13 +269,63 @@ def test_all_zero_bytes_0x55_and_vllm_floor_0x5e():
     assert np.all(gs.reshape(14, 8)[:, :5] == 0x5E5E5E5E)
 
 
-@pytest.mark.parametrize("eps", [1e-24, 1e-10, 1e-4, 1.0, 1e20])
+@pytest.mark.parametrize("eps", [2.0 ** -140, 1e-38, 1.1754943508222875e-38, 1e-30, 1e-24,
+                                 1e-10, 1e-4, 1.0, 1e20])
 def test_eps_range(eps):
+    """eps from the smallest accepted (2^-140, where an all-zero group's scale is a
+    subnormal) through FLT_MIN and 1e-30 to large values; groups of zeros and of tiny
+    values (bf16 subnormals included) take the kernel's IEEE-division path below an amax of
+    1e-24, in the same warps as ordinary groups."""
     x = synth.sweep_input(5, 64, 1024, torch.bfloat16)
     x[3] = 0
     x[5, :128] = 1e-30
+    x[6, 128:256] = 2.0 ** -133
+    x[7, 256:384] = torch.linspace(-1e-36, 1e-36, 128)
+    x[8, :16] = 0
     for fmt in FMTS:
-        compare(x, Case(eps=eps, scale_fmt=fmt))
+        for out in (P.E4M3, P.INT8):
+            compare(x, Case(eps=eps, scale_fmt=fmt, out_dtype=out, group=16 if fmt == 0 else 128))
+    compare(x, Case(eps=eps, flags=P.FLAG_UE8M0_SCALE_FLOOR, scale_fmt=P.SCALE_UE8M0_PACKED,
+                    layout=P.COL_MAJOR_TMA))
+    xs = torch.cat([x, x.flip(0)], 1)
+    compare(xs, Case(eps=eps, silu=True, scale_fmt=P.SCALE_UE8M0_PACKED), exact_silu=True)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_nonfinite_amax_fixture_and_overflowing_silu(fmt):
+    """Groups whose amax is +inf (an infinite element, or a silu product of finite gates
+    and ups that overflows binary32): the hand-worked fixture of tests/golden/, then a
+    larger call that mixes such groups with ordinary ones in every warp, flat and masked,
+    bf16 and fp16, e4m3 and int8."""
+    from golden_fixtures import nonfinite_amax_cases
+    key = {P.SCALE_FP32: "fp32", P.SCALE_UE8M0_PACKED: "packed", P.SCALE_UE8M0_FP32: "ue8m0_fp32"}[fmt]
+    for c in nonfinite_amax_cases():
+        x = torch.from_numpy(c["x"].view(np.int16).copy()).view(torch.bfloat16).reshape(1, -1)
+        case = Case(group=c["group"], silu=bool(c["silu"]), scale_fmt=fmt,
+                    out_dtype=P.E4M3 if c["out"] == "e4m3" else P.INT8)
+        gq, gs = compare(x, case)
+        assert np.array_equal(gq, c["codes"]) and np.array_equal(gs, c[key]), c["name"]
+    g = torch.Generator().manual_seed(17)
+    for dt in (torch.bfloat16, torch.float16):
+        big = torch.finfo(dt).max
+        gate = torch.randn((96, 1024), generator=g)
+        up = torch.randn((96, 1024), generator=g)
+        rows = torch.randint(0, 96, (40,), generator=g)
+        cols = torch.randint(0, 1024, (40,), generator=g)
+        gate[rows, cols] = big          # silu(g) = g, and g * up overflows unless |up| < 1
+        up[rows, cols] = big * torch.sign(torch.randn(40, generator=g))
+        x = torch.cat([gate, up], 1).to(dt)
+        for out in (P.E4M3, P.INT8):
+            compare(x, Case(silu=True, scale_fmt=fmt, out_dtype=out, group=64), exact_silu=True)
+        xi = torch.randn((64, 2048), generator=g)
+        xi[torch.randint(0, 64, (30,), generator=g), torch.randint(0, 2048, (30,), generator=g)] = \
+            float("inf")
+        xi[5, 7] = -float("inf")
+        xi = xi.to(dt)
+        for out in (P.E4M3, P.INT8):
+            compare(xi, Case(scale_fmt=fmt, out_dtype=out, layout=P.COL_MAJOR_TMA))
+            compare(xi.reshape(4, 16, 2048), Case(scale_fmt=fmt, out_dtype=out),
+                    masked_m=np.array([16, 3, 0, 9], np.int32))
 
 
 def test_extreme_values():

@@ -120,3 +120,55 @@ def test_hint_prefetch_stays_inside_x():
         off = (e * rows + row) * in_row + (g << (4 + lg_log2)) + (local & ((1 << lg_log2) - 1)) * 16
         end = off + (H if silu else 0) + 16
         assert np.all(row[go] < rows) and np.all(end[go] <= E * rows * in_row)
+
+
+def _magic(d: int) -> int:
+    return 0xFFFFFFFF if d == 1 else (1 << 32) // d
+
+
+def test_requant_chunks_stay_inside_and_cover_every_live_row_once():
+    """ptgq_next.cu, requant_kernel: lane chunks are numbered over row slots S = r * E + e
+    (row-major over (row, expert)), and a warp's task loop ends at the tasks that can hold
+    the first max(masked_m) * E slots.  Over shapes, group sizes, chunk widths, live counts
+    (empty, partial, full, out of range) and grids smaller and larger than the work: every
+    live chunk's code range and scale indices lie inside x / x_scale, and the live chunks
+    are exactly the chunks of rows r < clamp(masked_m[e], 0, m), each taken once."""
+    rng = np.random.default_rng(5)
+    for E, m, k, G, V, grid_warps in itertools.product(
+            [1, 3, 8, 33], [1, 5, 64], [16, 48, 128, 1152, 3584], [16, 32, 64, 128], [16, 32],
+            [8, 200]):
+        if k % G or k % V:
+            continue
+        mm = rng.integers(-2, m + 3, E).astype(np.int64)
+        mm[0] = m
+        live = np.clip(mm, 0, m)
+        max_live = int(live.max())
+        cpr = k // V
+        live_chunks = max_live * E * cpr
+        tasks = (live_chunks + 31) >> 5
+        # every chunk index a warp forms: tasks t < tasks, lanes 0..31 (any grid covers
+        # t = warp + j * grid_warps for all t < tasks)
+        t = np.arange(tasks, dtype=np.int64)
+        assert np.array_equal(np.unique(np.concatenate(
+            [np.arange(w, tasks, grid_warps) for w in range(min(grid_warps, max(tasks, 1)))] or
+            [np.zeros(0, np.int64)])), t)
+        c = ((t[:, None] << 5) + np.arange(32)).ravel()
+        assert c.max(initial=0) < 2 ** 32
+        S = _udiv(c, cpr, _magic(cpr))
+        assert np.array_equal(S, c // cpr)
+        col = c - S * cpr
+        r = _udiv(S, E, _magic(E))
+        assert np.array_equal(r, S // E)
+        e = S - r * E
+        ok = (c < live_chunks) & (r < live[np.minimum(e, E - 1)]) & (e < E)
+        off = (e * m + r) * k + col * V
+        assert np.all(off[ok] >= 0) and np.all(off[ok] + V <= E * m * k)
+        assert np.all(off[ok] % V == 0)
+        g = (col * V) >> int(np.log2(G))
+        g1 = g + (1 if (V == 32 and G == 16) else 0)
+        assert np.all(g1[ok] < k // G)
+        got = np.sort(off[ok])
+        want = np.sort(np.concatenate([(ee * m + rr) * k + np.arange(cpr) * V
+                                       for ee in range(E) for rr in range(int(live[ee]))] or
+                                      [np.zeros(0, np.int64)]))
+        assert np.array_equal(got, want), (E, m, k, G, V)
