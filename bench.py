@@ -7,10 +7,11 @@ e4m3 codes, UE8M0 exponents packed four per int32 in the TMA-aligned column-majo
 
 Prints one JSON line.  ``value`` is the achieved HBM throughput in GB/s (algorithmic bytes:
 input read + codes written + scale words written, per call, over the device time of the
-timed steps, summed over ranks).  Timing: W warm-up steps, then K steps replayed from a
-CUDA graph, bracketed by barrier + synchronize, timed with CUDA events on the launching
-stream; inputs rotate over buffer sets that together exceed 2.5x L2, so each call reads
-from HBM, not L2.
+timed steps, summed over ranks).  Timing: W warm-up calls, then five timed regions of
+exactly K calls each, replayed from CUDA graphs, each bracketed by an L2 flush, a barrier and
+a synchronize and timed with CUDA events on the launching stream; the median region (max
+over ranks) is reported.  Inputs rotate over buffer sets that together exceed 2.5x L2, so
+each call reads from HBM, not L2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -37,9 +38,12 @@ METRIC = "achieved HBM GB/s (% of GB300 peak) and µs/call, per_token_group_quan
 WORKLOAD = "flat bf16 x[4096,7168] N(0,1)+0.1% outliers x100+1% zero groups, G=128, e4m3, " \
            "UE8M0 packed int32 col-major (mn padded to 4, pads zero-filled)"
 T, H, G = 4096, 7168, 128
-GRAPH_CALLS = 400                      # calls captured per CUDA graph
+GRAPH_CALLS = 400                      # most calls captured in one CUDA graph
+REPEATS = 5                            # timed regions; the median is reported
 KERNEL_SOURCES = ["ptgq_kernel.cuh", "ptgq_math.cuh", "ptgq_api.cu", "ptgq_internal.h",
-                  "ptgq_inst_bf16_flat.cu", "ptgq_device.cuh", "silu_tables.inc"]
+                  "ptgq_inst_bf16_flat.cu", "ptgq_inst_bf16_masked.cu", "ptgq_inst_fp16_flat.cu",
+                  "ptgq_inst_fp16_masked.cu", "ptgq_device.cuh", "ptgq_next.cu",
+                  "silu_tables.inc"]
 
 
 def algorithmic_bytes(tokens: int = T, hidden: int = H, group: int = G) -> int:
@@ -49,8 +53,8 @@ def algorithmic_bytes(tokens: int = T, hidden: int = H, group: int = G) -> int:
 
 
 def kernel_source_sha() -> str:
-    """Hash of the benchmarked kernel's sources with comments and blank space removed, so a
-    recorded DRAM traffic figure stays valid across comment-only edits and no longer."""
+    """Hash of the kernel sources with comments and blank space removed, so a recorded DRAM
+    traffic figure stays valid across comment-only edits and no longer."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "fp8_token_group_gb300", "csrc", f)) as fh:
@@ -71,17 +75,19 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel."""
+def recorded_traffic(workload: str):
+    """Steady-state DRAM bytes per launch of a workload's kernel from the committed ncu
+    record (mean over back-to-back launches), if it was taken on the current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_source_sha") != kernel_source_sha() or d.get("workload") != "flat_outliers":
+    if d.get("kernel_source_sha") != kernel_source_sha():
         return None
-    return d.get("dram_bytes_per_launch")
+    w = d.get("workloads", {}).get(workload)
+    return None if w is None else w.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -240,10 +246,10 @@ def cpu_baseline(x_cpu, budget_s: float = 8.0) -> dict:
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
-    from fp8_token_group_gb300 import synth
     import oracle as O
     O.build()
-    x = synth.flat_outliers()
+    wl = workloads()["flat_outliers"]
+    x, _ = wl.inputs()
     # size each step so the whole run stays within about a minute
     cores = host_cores()
     el1, _ = oracle_rate(x, cores, 2, 1, threads=cores)
@@ -255,10 +261,10 @@ def run_reference(args, world, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
+        "config": bench_config(wl, x, None, world),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows} rows x {H} per step in {cores} row blocks on "
-                                   f"{cores} threads, C++ oracle"},
+                         "sample": f"each step: {rows} of the workload's {T} rows x {H}, in "
+                                   f"{cores} row blocks on {cores} threads, C++ oracle"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -418,12 +424,18 @@ def workloads():
 
 # ---------------------------------------------------------------- GPU timing
 
-def build_sets(P, wl, x_cpu, mm_cpu, device):
-    """Enough buffer sets (each with its own input copy) that together they exceed L2 2.5x."""
-    per_set = wl.bytes_per_call(x_cpu, mm_cpu)
+def nsets_for(per_set: int) -> int:
+    """Buffer sets (each with its own input) that together exceed 2.5x the L2 size; a
+    divisor of GRAPH_CALLS."""
     nsets = max(2, min(GRAPH_CALLS, -(-int(2.5 * L2_BYTES) // max(per_set, 1))))
     while GRAPH_CALLS % nsets:
         nsets += 1
+    return nsets
+
+
+def build_sets(P, wl, x_cpu, mm_cpu, device):
+    """Enough buffer sets (each with its own input copy) that together they exceed L2 2.5x."""
+    nsets = nsets_for(wl.bytes_per_call(x_cpu, mm_cpu))
     mm = None if mm_cpu is None else mm_cpu.to(device)
     if mm is not None and x_cpu.shape[1] > VIEW_SETS_PER_BUFFER and \
             nsets * x_cpu.numel() * 2 > 8 * 2 ** 30:
@@ -471,9 +483,68 @@ def build_view_sets(P, wl, x_cpu, mm, device, nsets):
     return sets
 
 
-def time_graph(P, wl, sets, steps: int, warmup: int, world: int, sampler=None):
-    """Capture GRAPH_CALLS calls (rotating buffer sets) and replay; returns elapsed s for
-    `steps` calls (rounded up to whole graphs), the number of calls made, and clocks."""
+def graph_plan(calls: int, nsets: int, cap: int = GRAPH_CALLS):
+    """How `calls` consecutive calls are replayed: (g, reps, r) with calls = r + reps * g.
+    The main graph holds g calls, a multiple of nsets (set i % nsets for call i), so it
+    starts at set 0 and ends at set nsets - 1; the remainder graph of r calls runs first
+    and uses sets (nsets - r + i) % nsets, so it also ends at set nsets - 1.  Consecutive
+    calls therefore always read different buffer sets."""
+    g = min(calls, cap) // nsets * nsets
+    if g == 0:
+        return 0, 0, calls
+    return g, calls // g, calls % g
+
+
+class GraphRunner:
+    """CUDA graphs of calls over rotating buffer sets, captured on demand by size."""
+
+    def __init__(self, P, wl, sets, stream):
+        self.P, self.wl, self.sets, self.stream = P, wl, sets, stream
+        self.graphs = {}
+
+    def _graph(self, n: int, first_set: int):
+        import torch
+        key = (n, first_set)
+        if key not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(n):
+                    self.wl.call(self.P, *self.sets[(first_set + i) % len(self.sets)])
+            self.graphs[key] = g
+        return self.graphs[key]
+
+    def enqueue(self, calls: int):
+        """Enqueue exactly `calls` calls on the runner's stream."""
+        nsets = len(self.sets)
+        g, reps, r = graph_plan(calls, nsets)
+        if r:
+            self._graph(r, (nsets - r) % nsets).replay()
+        for _ in range(reps):
+            self._graph(g, 0).replay()
+
+    def prepare(self, calls: int):
+        nsets = len(self.sets)
+        g, reps, r = graph_plan(calls, nsets)
+        if r:
+            self._graph(r, (nsets - r) % nsets)
+        if reps:
+            self._graph(g, 0)
+
+
+def flush_l2(device):
+    """Overwrite a buffer twice the L2 size so the next region starts with a cold cache."""
+    import torch
+    buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    buf.fill_(1)
+    del buf
+
+
+def time_graph(P, wl, sets, steps: int, warmup: int, world: int, sampler=None,
+               repeats: int = REPEATS):
+    """`warmup` untimed calls, then `repeats` timed regions of exactly `steps` calls each
+    (CUDA graphs over rotating buffer sets), each region bracketed by an L2 flush, a
+    barrier and a synchronize, timed with CUDA events on the launching stream.  Returns the
+    per-region elapsed seconds (max over ranks) and the clock record."""
     import torch
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
@@ -481,31 +552,37 @@ def time_graph(P, wl, sets, steps: int, warmup: int, world: int, sampler=None):
         for i in range(min(8, len(sets))):
             wl.call(P, *sets[i])
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(GRAPH_CALLS):
-            wl.call(P, *sets[i % len(sets)])
-    reps = max(1, -(-steps // GRAPH_CALLS))
-    wreps = max(1, -(-warmup // GRAPH_CALLS))
+    runner = GraphRunner(P, wl, sets, stream)
+    runner.prepare(steps)
+    runner.prepare(warmup)
     with torch.cuda.stream(stream):
-        for _ in range(wreps):
-            g.replay()
+        runner.enqueue(warmup)
     torch.cuda.synchronize()
+    device = torch.cuda.current_device()
     if sampler:
         sampler.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(reps):
-            g.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    regions = []
+    for _ in range(repeats):
+        flush_l2(device)
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            # keep the GPU busy while the host enqueues the region, so the first call
+            # follows the start event without a launch gap
+            if hasattr(torch.cuda, "_sleep"):
+                torch.cuda._sleep(200_000)
+            start.record(stream)
+            runner.enqueue(steps)
+            end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        regions.append(reduce_max(start.elapsed_time(end) / 1e3, world,
+                                  torch.device("cuda", device)))
     clocks = sampler.stop() if sampler else None
-    del g
-    return start.elapsed_time(end) / 1e3, reps * GRAPH_CALLS, clocks
+    runner.graphs.clear()
+    return regions, clocks
 
 
 def time_e2e(P, wl, x_cpu, mm_cpu, steps: int, device):
@@ -592,17 +669,105 @@ def time_e2e_zero_copy(P, wl, x_cpu, mm_cpu, steps: int, device):
     return el, xh.numel() * xh.element_size(), qh.numel() * qh.element_size() + sh.numel() * sh.element_size()
 
 
-def measure_device(P, wl, device, steps: int) -> dict:
+def measure_device(P, wl, device, steps: int, inputs=None, repeats: int = 3) -> dict:
+    """One workload timed like the benchmark line (median of `repeats` regions)."""
     import torch
-    x, mm = wl.inputs()
+    x, mm = inputs if inputs is not None else wl.inputs()
     sets = build_sets(P, wl, x, mm, device)
-    el, calls, _ = time_graph(P, wl, sets, steps, 100, 1)
+    regions, _ = time_graph(P, wl, sets, steps, 100, 1, repeats=repeats)
     nb = wl.bytes_per_call(x, mm)
-    us = el / calls * 1e6
+    us = statistics.median(regions) / steps * 1e6
     del sets
     torch.cuda.empty_cache()
+    peak, _ = measured_peak()
     return {"desc": wl.desc, "us_per_call": round(us, 3), "bytes_per_call": nb,
-            "gbs": round(nb / us / 1e3, 1), "live_rows": wl.live_rows(x, mm)}
+            "gbs": round(nb / us / 1e3, 1), "pct_of_peak": round(100 * nb / us / 1e3 / peak, 1),
+            "live_rows": wl.live_rows(x, mm)}
+
+
+class CopyWorkload(Workload):
+    """A device-to-device copy (torch's copy kernel) of half a call's algorithmic bytes, so
+    that it reads and writes the same total: the memory system's floor for one launch
+    moving that much, as a reference point beside the quantizer."""
+
+    def __init__(self, nbytes: int):
+        super().__init__("copy_reference", f"torch copy_ of {nbytes // 2} bytes (reads + writes "
+                         f"{nbytes} bytes)", None)
+        self.nbytes = nbytes
+
+    def inputs(self):
+        import torch
+        return torch.zeros(self.nbytes // 2, dtype=torch.uint8), None
+
+    def live_rows(self, x, mm):
+        return 0
+
+    def bytes_per_call(self, x, mm):
+        return 2 * x.numel()
+
+    def alloc(self, P, xd, mm):
+        import torch
+        return torch.empty_like(xd), None
+
+    def call(self, P, xd, q, s, mm=None):
+        q.copy_(xd)
+
+
+# The large-token shapes of the sweep timed in the benchmark line: T in {4096, 32768} x H in
+# {2048, 4096, 7168} x G in {16, 128}, bf16 -> e4m3, plus one fp16 and one int8 shape per T;
+# fp32 row-major scales.
+LARGE_SWEEP = ([(T, H, "bfloat16", G, "e4m3") for T in (4096, 32768) for H in (2048, 4096, 7168)
+                for G in (16, 128)] +
+               [(T, 4096, "float16", 64, "e4m3") for T in (4096, 32768)] +
+               [(T, 2048, "bfloat16", 32, "int8") for T in (4096, 32768)])
+
+
+def large_sweep(P, device, steps: int, copy_reference: bool = True):
+    """The LARGE_SWEEP shapes (inputs of the sweep's recipe, drawn with the seed of the
+    shape's G = 16, e4m3 case and shared by its group sizes), each with the quantizer's time
+    and, for T = 4096, a copy of equal traffic as the floor reference."""
+    import torch
+    from fp8_token_group_gb300 import synth
+    peak, _ = measured_peak()
+    index = {(T, H, str(dt)[6:], G, out): i for i, T, H, dt, G, out in synth.sweep_cases()}
+    rows, inputs = [], {}
+    for T, H, dt, G, out in LARGE_SWEEP:
+        key = (T, H, dt)
+        if key not in inputs:
+            inputs.clear()
+            inputs[key] = synth.sweep_input(index[(T, H, dt, 16, "e4m3")], T, H,
+                                            getattr(torch, dt))
+        x = inputs[key]
+        name = f"{T}x{H}-{dt}-G{G}-{out}"
+        wl = Workload(name, name, None, group=G, out=0 if out == "e4m3" else 1)
+        r = measure_device(P, wl, device, steps, inputs=(x, None))
+        line = {"tokens": T, "hidden": H, "dtype": dt, "group": G, "out": out,
+                "us_per_call": r["us_per_call"], "gbs": r["gbs"], "pct_of_peak": r["pct_of_peak"]}
+        if copy_reference and T == 4096:
+            c = measure_device(P, CopyWorkload(r["bytes_per_call"]), device, steps)
+            line["copy_reference"] = {"us_per_call": c["us_per_call"], "gbs": c["gbs"],
+                                      "pct_of_peak": c["pct_of_peak"]}
+        rows.append(line)
+    pcts = [r["pct_of_peak"] for r in rows]
+    summary = {"configs": len(rows), "min_pct": min(pcts), "median_pct": statistics.median(pcts),
+               "at_or_above_75_pct": sum(p >= 75 for p in pcts),
+               "peak_gbs": peak, "timing": f"median of 3 regions of {steps} calls each"}
+    return rows, summary
+
+
+def bench_config(wl, x, mm, world: int) -> dict:
+    """The `config` object of the JSON line (shared by both arms)."""
+    bpc = wl.bytes_per_call(x, mm)
+    nsets = nsets_for(bpc)
+    return {"workload": wl.desc, "global_batch": wl.live_rows(x, mm) * world,
+            "group_size": wl.group, "input": "bf16", "output": "e4m3",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": f"{nsets} rotating buffer sets, each with its own input, together "
+                  f"{nsets * bpc / 1e6:.0f} MB > 2.5x the 129 MB L2; L2 flushed before "
+                  f"each timed region",
+            "timing": f"median of {REPEATS} timed regions of exactly `steps` calls, CUDA "
+                      f"graphs of up to {GRAPH_CALLS} calls, CUDA events on the launching "
+                      f"stream"}
 
 
 def run_ours(args, world, rank, local):
@@ -616,17 +781,17 @@ def run_ours(args, world, rank, local):
     wl = wls[args.workload]
     x, mm = wl.inputs()
     sets = build_sets(P, wl, x, mm, device)
-    nsets = len(sets)
     sampler = ClockSampler(local) if rank == 0 else None
-    elapsed, calls, clocks = time_graph(P, wl, sets, args.steps, args.warmup, world, sampler)
+    regions, clocks = time_graph(P, wl, sets, args.steps, args.warmup, world, sampler)
     del sets
     torch.cuda.empty_cache()
-    max_el = reduce_max(elapsed, world, device)
+    steps = args.steps
+    el = statistics.median(regions)               # max over ranks, median over regions
     bpc = wl.bytes_per_call(x, mm)
-    value = aggregate(bpc, calls, world, max_el)
-    us = max_el / calls * 1e6
+    value = aggregate(bpc, steps, world, el)
+    us = el / steps * 1e6
     peak, peak_kind = measured_peak()
-    achieved = bpc / (elapsed / calls) / 1e9      # this rank's launches, per launch
+    achieved = bpc / (el / steps) / 1e9
 
     e2e_steps = max(3, min(args.steps, 50))
     copy_el, h2d, d2h = time_e2e(P, wl, x, mm, e2e_steps, device)
@@ -637,12 +802,13 @@ def run_ours(args, world, rank, local):
         zc_el = reduce_max(zc_el, world, device)
     e2e_mode = "zero-copy" if zc_el is not None and zc_el < copy_el else "copies"
     e2e_el = zc_el if e2e_mode == "zero-copy" else copy_el
-    e2e_gbs = lambda el: None if el is None else round(world * e2e_steps * bpc / el / 1e9, 2)
-    others = {}
+    e2e_gbs = lambda t: None if t is None else round(world * e2e_steps * bpc / t / 1e9, 2)
+    others, sweep_rows, sweep_summary = {}, None, None
     if rank == 0 and not args.no_extra:
         for name, other in wls.items():
             if name != wl.name:
                 others[name] = measure_device(P, other, device, 4000)
+        sweep_rows, sweep_summary = large_sweep(P, device, 2000)
     base = cpu_baseline(x) if (rank == 0 and world == 1 and not args.no_cpu
                                and wl.name == "flat_outliers") else None
     live = wl.live_rows(x, mm)
@@ -650,26 +816,26 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
-            "steps": calls, "warmup": args.warmup, "ms_per_step": round(max_el / calls * 1e3, 6),
+            "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": wl.desc, "global_batch": live * world, "group_size": wl.group,
-                       "input": "bf16", "output": "e4m3",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": f"{nsets} rotating buffer sets, each with its own input, "
-                             f"together {nsets * bpc / 1e6:.0f} MB > 2.5x the 129 MB L2",
-                       "timing": f"CUDA graph of {GRAPH_CALLS} calls replayed, CUDA events"},
+            "config": bench_config(wl, x, mm, world),
             "us_per_call": round(us, 3),
-            "tokens_per_s": round(world * live * calls / max_el, 1),
+            "tokens_per_s": round(world * live * steps / el, 1),
             "pct_of_peak": round(100 * achieved / peak, 2),
+            "regions_ms": [round(r * 1e3, 5) for r in regions],
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "traffic": recorded_traffic() if wl.name == "flat_outliers" else None,
+                         "traffic": recorded_traffic(wl.name),
+                         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum "
+                                           "per launch, mean over back-to-back launches "
+                                           "(profiles/traffic.json), when taken on the "
+                                           "current kernel sources",
                          "algorithmic_bytes_per_launch": bpc},
             "clocks": clocks,
-            "gpu_launches": calls,
+            "gpu_launches": steps,
             "e2e": {"value": e2e_gbs(e2e_el), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "mode": e2e_mode, "copies_gbs": e2e_gbs(copy_el),
@@ -683,6 +849,8 @@ def run_ours(args, world, rank, local):
                      "wall clock over all steps")},
             "cpu_baseline": base,
             "other_workloads": others,
+            "large_sweep": sweep_rows,
+            "large_sweep_summary": sweep_summary,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -710,9 +878,9 @@ def run_sweep(args, out_path=None):
             continue
         x = synth.sweep_input(idx, T, H, dt)
         name = f"{T}x{H}-{str(dt)[6:]}-G{G}-{out}"
-        wl = Workload(name, name, lambda x=x: x, group=G, out=0 if out == "e4m3" else 1)
-        r = measure_device(P, wl, device, args.sweep_steps)
-        pct = round(100 * r["gbs"] / peak, 1)
+        wl = Workload(name, name, None, group=G, out=0 if out == "e4m3" else 1)
+        r = measure_device(P, wl, device, args.sweep_steps, inputs=(x, None))
+        pct = r["pct_of_peak"]
         line = {"sweep": idx, "tokens": T, "hidden": H, "dtype": str(dt)[6:], "group": G,
                 "out": out, "us_per_call": r["us_per_call"], "gbs": r["gbs"],
                 "pct_of_peak": pct}
@@ -757,7 +925,7 @@ def main():
         return run_sweep(args, args.sweep_out)
     if args.impl == "reference":
         # the CPU oracle: rank 0 alone runs it, other ranks exit without work
-        return run_reference(args, int(os.environ.get("WORLD_SIZE", "1")),
+        return run_reference(args, int(os.environ.get("WORLD_SIZE", str(args.gpus))),
                              int(os.environ.get("RANK", "0")))
     world, rank, local = dist_setup(args.gpus)
     return run_ours(args, world, rank, local)

@@ -202,12 +202,8 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   p.eps = eps;
   p.fmax = out_dtype == PTGQ_E4M3 ? 448.0f : 127.0f;
   p.scale_floor = (flags & PTGQ_FLAG_UE8M0_SCALE_FLOOR) ? 1e-10f : 0.0f;
-  // Live rows per expert that the prefetch of the first rows guesses: the caller's hint,
-  // or one row per expert without a hint (the first row of an expert is live whenever the
-  // expert has any row, which covers the decode-sized calls where the prefetch matters).
-  p.rows_hint = !masked ? 0u
-                        : static_cast<uint32_t>(std::min<int64_t>(expected_m > 0 ? expected_m : 1,
-                                                                  g.rows));
+  p.rows_hint = masked && expected_m > 0
+                    ? static_cast<uint32_t>(std::min<int64_t>(expected_m, g.rows)) : 0u;
   p.rows_hint_magic = p.rows_hint <= 1u ? 0xFFFFFFFFu
                                         : static_cast<uint32_t>((uint64_t(1) << 32) / p.rows_hint);
   if (!masked) {

@@ -55,9 +55,8 @@ struct Params {
   float fmax;                // 448 (e4m3) or 127 (int8)
   float scale_floor;         // UE8M0 only: s = max(s, scale_floor); 1e-10 for the vLLM
                              // semantics, else 0 (a no-op since s > 0)
-  uint32_t rows_hint;        // masked: the live rows per expert that the prefetch of each
-                             // warp's first rows guesses: min(expected_m, rows), or 1
-                             // without a hint; 0 in flat calls
+  uint32_t rows_hint;        // masked: the caller's expected live rows per expert,
+                             // min(expected_m, rows); 0 without a hint
   uint32_t rows_hint_magic;  // floor(2^32 / rows_hint), or 0xFFFFFFFF when rows_hint <= 1
   // Flat zero-fill of padding (rows [T, rows) of q; scale rows past T).
   int64_t zero_q_begin;      // byte offsets into q, multiples of 16

@@ -127,9 +127,11 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   int32_t* bucket = prefix + (p.n + 1);
   uint32_t bshift = 0u;
   if constexpr (kMasked) {
-    // The rows of this warp's first task, guessed as if every expert had exactly rows_hint
-    // live rows (the caller's expected_m, else one), go to L2 while masked_m is read
-    // (hinted decode batch, bf16 silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us).
+    // With a hint of the live rows per expert, the rows of this warp's first task, guessed
+    // as if every expert had exactly rows_hint live rows, go to L2 while masked_m is read
+    // (hinted decode batch, bf16 silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us).  Calls
+    // without a hint prefetch nothing: a guess of one row per expert gained 0.08 us on the
+    // unhinted decode batch but cost 0.15-0.18 us on the large masked silu calls.
     // The guess only decides what is prefetched: rows below rows_hint <= rows of experts
     // below n, so every prefetched address lies inside x.
     if (p.rows_hint > 0u) {

@@ -523,19 +523,13 @@ struct PtShape {
 // rounds * (warps per SM), with the CTAs of the grid spread evenly over the SMs; the shape
 // minimizing that product wins, ties going to more warps in total.  One buffer per warp
 // is allowed only when every warp takes at most one row (nothing to overlap).  Returns
-// false when no shape fits.  PTGQ_PT_FORCE_BUFS / _WARPS restrict the choice (sweeps).
+// false when no shape fits.
 bool per_token_shape(int dtype, int64_t tokens, int64_t row_bytes, PtShape* out) {
   constexpr int64_t kMaxSmem = 227 * 1024;
   int64_t best_cost = -1, best_total = 0;
   for (int bufs = 2; bufs >= 1; --bufs) {
-#ifdef PTGQ_PT_FORCE_BUFS
-    if (bufs != PTGQ_PT_FORCE_BUFS) continue;
-#endif
     const void* fn = per_token_smem_fn(dtype, bufs);
     for (int wc = 1; wc <= kWarps; ++wc) {
-#ifdef PTGQ_PT_FORCE_WARPS
-      if (wc != PTGQ_PT_FORCE_WARPS) continue;
-#endif
       const int64_t smem = static_cast<int64_t>(wc) * bufs * row_bytes;
       if (smem > kMaxSmem) break;
       int bps = 0, sms = 0;

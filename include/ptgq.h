@@ -163,9 +163,9 @@ enum {
  *               the grid is sized for every row of tokens_pad being live; with one it is
  *               sized for E * min(expected_m, tokens_pad) rows.  Results are the same for
  *               any value: the grid strides over whatever rows are live, so a low hint
- *               costs time, never correctness.  Rows below min(expected_m, tokens_pad)
- *               of x (below 1 without a hint) may be prefetched into L2 before the live
- *               counts are known (a cache hint: their contents never reach the
+ *               costs time, never correctness.  With a hint, rows below
+ *               min(expected_m, tokens_pad) of x may be prefetched into L2 before the
+ *               live counts are known (a cache hint: their contents never reach the
  *               outputs), so x must span its whole [E, tokens_pad, H_in] extent, as
  *               ptgq_quant requires.  0: no hint.  Ignored in flat mode.
  *               Negative: PTGQ_ERR_SHAPE. */

@@ -66,3 +66,17 @@ def test_full_copies_for_other_masked_workloads():
     per = wl.bytes_per_call(x, mm)
     nsets = max(2, min(bench.GRAPH_CALLS, -(-int(2.5 * bench.L2_BYTES) // per)))
     assert nsets * x.numel() * 2 <= 8 * 2 ** 30      # below the view-set threshold
+
+
+@pytest.mark.parametrize("nsets", [2, 4, 5, 8, 200, 400])
+def test_graph_plan_runs_exact_calls_on_alternating_sets(nsets):
+    """bench.py runs exactly the requested calls, and within a timed region no call reads the
+    buffer set the call before it read (so each reads from HBM): over call counts below, at
+    and above the graph size.  Between regions bench.py flushes L2."""
+    for calls in [1, 2, 3, 5, 19, 20, 21, 399, 400, 401, 1003, 60000]:
+        g, reps, r = bench.graph_plan(calls, nsets)
+        assert r + reps * g == calls and g % nsets == 0 and g <= bench.GRAPH_CALLS
+        seq = [(nsets - r + i) % nsets for i in range(r)] + [i % nsets for i in range(g)] * reps
+        assert len(seq) == calls
+        assert all(a != b for a, b in zip(seq, seq[1:]))
+        assert seq[-1] == nsets - 1
