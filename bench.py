@@ -803,11 +803,18 @@ def run_ours(args, world, rank, local):
     e2e_mode = "zero-copy" if zc_el is not None and zc_el < copy_el else "copies"
     e2e_el = zc_el if e2e_mode == "zero-copy" else copy_el
     e2e_gbs = lambda t: None if t is None else round(world * e2e_steps * bpc / t / 1e9, 2)
-    others, sweep_rows, sweep_summary = {}, None, None
+    others, sweep_rows, sweep_summary, copy_ref = {}, None, None, None
     if rank == 0 and not args.no_extra:
+        c = measure_device(P, CopyWorkload(bpc), device, 4000)
+        copy_ref = {"us_per_call": c["us_per_call"], "gbs": c["gbs"],
+                    "pct_of_peak": c["pct_of_peak"], "desc": c["desc"]}
         for name, other in wls.items():
             if name != wl.name:
-                others[name] = measure_device(P, other, device, 4000)
+                r = measure_device(P, other, device, 4000)
+                c = measure_device(P, CopyWorkload(r["bytes_per_call"]), device, 4000)
+                r["copy_reference"] = {"us_per_call": c["us_per_call"], "gbs": c["gbs"],
+                                       "pct_of_peak": c["pct_of_peak"]}
+                others[name] = r
         sweep_rows, sweep_summary = large_sweep(P, device, 2000)
     base = cpu_baseline(x) if (rank == 0 and world == 1 and not args.no_cpu
                                and wl.name == "flat_outliers") else None
@@ -848,6 +855,7 @@ def run_ours(args, world, rank, local):
                      "and scales -> pinned host; double-buffered on H2D/compute/D2H streams, "
                      "wall clock over all steps")},
             "cpu_baseline": base,
+            "copy_reference": copy_ref,
             "other_workloads": others,
             "large_sweep": sweep_rows,
             "large_sweep_summary": sweep_summary,

@@ -277,7 +277,11 @@ struct RequantParams {
   uint32_t g_log2;               // log2(group size)
 };
 
-constexpr int kRequantBlocksPerSm = 4;
+// CTAs of 8 warps per SM (the grid is at most this many per SM): with the speculative
+// prefetch below, a wave of three reaches only rows that are live in the page's shape (8
+// experts, 128 of 1024 rows live: 2.77 us, against 3.03 us with four CTAs per SM, whose
+// first wave also prefetches dead rows, and 3.29 us with four and no prefetch).
+constexpr int kRequantBlocksPerSm = 3;
 
 // Requantizes kV codes (kV = 32, or 16 when k is not a multiple of 32) of one row per lane.
 //
@@ -297,6 +301,23 @@ __global__ void __launch_bounds__(kThreads, kRequantBlocksPerSm) requant_kernel(
   griddep_wait();
   griddep_launch_dependents();
   const uint32_t lane = threadIdx.x & 31u;
+  // Speculative prefetch: this lane's chunk of the warp's first task, as if every row were
+  // live, goes to L2 while masked_m and the output scale are read, so the row loads that
+  // follow mostly hit L2 instead of waiting for a second DRAM round trip.  Slots are
+  // numbered rows first, so the first wave covers the first rows of every expert, which
+  // are the live ones unless an expert has fewer live rows than the wave reaches; a
+  // prefetch of a dead row only costs a wasted read (at most 32 bytes per lane of the
+  // first wave: 2.5 MB on 152 SMs).  Every prefetched address lies inside x (r < m).
+  {
+    const uint32_t c0 = ((blockIdx.x * kWarps + (threadIdx.x >> 5)) << 5) + lane;
+    const uint32_t S0 = udiv(c0, p.cpr, p.cpr_magic);
+    const uint32_t r0 = udiv(S0, p.experts, p.e_magic);
+    if (r0 < p.m) {
+      const uint32_t e0 = S0 - r0 * p.experts;
+      prefetch_l2(p.x + (static_cast<int64_t>(e0) * p.m + r0) * p.k +
+                  static_cast<int64_t>(c0 - S0 * p.cpr) * kV);
+    }
+  }
   const float oscale = *p.output_scale;                 // in flight with masked_m
   const bool masked = p.masked_m != nullptr;
   // Live rows of expert `lane` (E <= 32), and the largest live count of any expert.
@@ -304,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, kRequantBlocksPerSm) requant_kernel(
   if (masked) {
     uint32_t mx = 0u;
     for (uint32_t e = lane; e < p.experts; e += 32u) {
-      const int32_t v = p.masked_m[e];
+      const int32_t v = __ldg(p.masked_m + e);
       const uint32_t c = v < 0 ? 0u : min(static_cast<uint32_t>(v), p.m);
       if (e == lane) my_live = c;
       mx = max(mx, c);
@@ -640,7 +661,10 @@ extern "C" int ptgq_requant_per_tensor(const void* x, const float* x_scale, int6
   const void* fn = wide ? reinterpret_cast<const void*>(&requant_kernel<32>)
                         : reinterpret_cast<const void*>(&requant_kernel<16>);
   const int64_t tasks = (num_experts * m * p.cpr + 31) / 32;
-  const int grid = grid_for(fn, 0, (tasks + kWarps - 1) / kWarps);
+  int bps = 0, sms = 0;
+  if (occupancy(fn, 0, kThreads, &bps, &sms) != 0) return PTGQ_ERR_CUDA;
+  const int64_t wave = static_cast<int64_t>(std::min(bps, kRequantBlocksPerSm)) * sms;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((tasks + kWarps - 1) / kWarps, wave)));
   if (grid < 0) return PTGQ_ERR_CUDA;
   void* args[] = {&p};
   return launch(fn, grid, 0, stream, args);
