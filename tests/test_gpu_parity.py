@@ -487,6 +487,12 @@ def test_binding_rejects_short_buffers_before_launch():
         P.quant(xmd, qm, sm, 128, fuse_silu=True, masked_m=mmd[:3], **kw)
     with pytest.raises(ValueError, match="out_s"):
         P.quant(xmd, qm, sm[:-1], 128, fuse_silu=True, masked_m=mmd, **kw)
+    xo = torch.zeros((4, 2 * 256 + 1), dtype=torch.bfloat16, device="cuda")    # odd width
+    with pytest.raises(ValueError, match="fuse_silu"):
+        P.quant(xo, q, s, 128, fuse_silu=True, **kw)
+    with pytest.raises(ValueError, match="fuse_silu"):
+        P.alloc_outputs(torch.zeros((4, 257), dtype=torch.bfloat16, device="cuda"), 128,
+                        fuse_silu=True)
     xt = torch.randn(16, 512, device="cuda").to(torch.bfloat16)
     qt = torch.empty((16, 512), dtype=torch.float8_e4m3fn, device="cuda")
     st = torch.empty(16, dtype=torch.float32, device="cuda")
