@@ -224,8 +224,8 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
   if (rc != PTGQ_OK) return rc;
 
-  // Persistent grid: at most one full wave, fewer when the work is small (masked: as
-  // small as the expected live rows need, when the caller gives a hint).
+  // Grid: at most one full wave, fewer when the work is small (masked: as small as the
+  // expected live rows need, when the caller gives a hint); the kernel strides over tasks.
   const int64_t lanes_per_unit = (int64_t(group_size) / 16) << g.ug_log2;
   const int64_t rows_hint = expected_m > 0 ? std::min<int64_t>(expected_m, g.rows) : g.rows;
   const int64_t units_max = (masked ? g.blocks * rows_hint : n) * g.upr;
@@ -240,12 +240,23 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   }
   const int per_cta = quant_small_tasks_per_cta(key.fp16 != 0, key.silu != 0);
   int64_t want = (tasks + per_cta - 1) / per_cta;
+  int64_t full = static_cast<int64_t>(per_sm) * sms;
+  // Large plain flat calls (more than 16 tasks per warp of one wave): CTAs of 8 tasks per warp
+  // instead of one persistent wave.  A persistent wave finishes unevenly (on each SM the CTA
+  // dispatched first ends about 1.4 us before the last one, and SMs differ by up to 2 us);
+  // with several waves of shorter CTAs the block scheduler hands the later CTAs to the SMs
+  // that free up first.  [32768, 7168]: 105.2 -> 103.9 us at G = 128, 123.7 -> 109.6 us at
+  // G = 16; [8192, 7168] G = 16: 30.2 -> 29.4 us.  Below the threshold (the benchmarked
+  // [4096, 7168] has 11.8 tasks per warp) one wave stays faster (14.9 against 15.7 us).
+  if (!masked && !fuse_silu && !key.light && tasks > 16 * full * kWarps) {
+    want = (tasks + per_cta * 8 - 1) / (per_cta * 8);
+    full = want;
+  }
   if (!masked) {
     const int64_t zero_chunks = (p.zero_q_end - p.zero_q_begin) / 16 + p.zero_s_rows * g.ncol;
     want = std::max<int64_t>(want, (zero_chunks + threads - 1) / threads);
   }
-  const int64_t full = static_cast<int64_t>(per_sm) * sms;
-  const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, full)));
+  const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(want, std::max(full, int64_t(1)))));
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);

@@ -116,6 +116,17 @@ def test_flat_light_and_standard_flavours(T, fmt, layout, out):
     compare(x, Case(scale_fmt=fmt, layout=layout, out_dtype=out, tokens_pad=T + 3))
 
 
+@pytest.mark.parametrize("fmt,layout,out", [(P.SCALE_FP32, P.ROW_MAJOR, P.E4M3),
+                                            (P.SCALE_UE8M0_PACKED, P.COL_MAJOR_TMA, P.E4M3),
+                                            (P.SCALE_UE8M0_FP32, P.COL_MAJOR_TMA, P.INT8)])
+def test_flat_multi_wave_grid(fmt, layout, out):
+    """Plain flat calls of more than 16 tasks per warp of one wave run a grid of several
+    waves of CTAs with 8 tasks per warp ([8192, 7168] has 23.6 per warp of a wave), padding
+    rows included: every output against the oracle."""
+    x = synth.flat_outliers(tokens=8192, hidden=7168)
+    compare(x, Case(scale_fmt=fmt, layout=layout, out_dtype=out, tokens_pad=8195))
+
+
 @pytest.mark.parametrize("expected_m", [1, 7, 200, 384, 100000])
 def test_masked_expected_m_hint_changes_nothing(expected_m):
     """A hint far below, near or above the live counts sizes the grid differently; the
