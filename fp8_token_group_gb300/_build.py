@@ -59,8 +59,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    r = subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs],
-                       capture_output=True, text=True)
+    # -Bsymbolic: the library's own references (kernel tables, template instances) bind to
+    # its own definitions even when another library in the process defines the same names.
+    r = subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-Bsymbolic",
+                        "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)

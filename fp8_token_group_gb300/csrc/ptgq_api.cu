@@ -219,7 +219,7 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   const size_t smem = dynamic_smem_bytes(key, masked ? n : 0);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PTGQ_ERR_CUDA;
-  const int threads = quant_threads(key.fp16 != 0, key.silu != 0);
+  const int threads = quant_threads(key.fp16 != 0, key.silu != 0, key.masked != 0);
   int per_sm = 0, sms = 0;
   rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
   if (rc != PTGQ_OK) return rc;
@@ -238,7 +238,7 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
     rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
     if (rc != PTGQ_OK) return rc;
   }
-  const int per_cta = quant_small_tasks_per_cta(key.fp16 != 0, key.silu != 0);
+  const int per_cta = quant_small_tasks_per_cta(key.fp16 != 0, key.silu != 0, key.masked != 0);
   int64_t want = (tasks + per_cta - 1) / per_cta;
   int64_t full = static_cast<int64_t>(per_sm) * sms;
   // Large plain flat calls (more than 16 tasks per warp of one wave): CTAs of 8 tasks per warp

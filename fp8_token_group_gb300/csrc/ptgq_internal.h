@@ -7,20 +7,24 @@
 
 namespace ptgq {
 
-constexpr int kThreads = 256;                 // 8 warps per CTA (all but the fp16 silu instances)
+constexpr int kThreads = 256;                 // 8 warps per CTA (the plain and flat silu instances)
 constexpr int kWarps = kThreads / 32;
 // Threads per CTA of a quantizer instance.  The fp16 fused-silu instances hold a 162 KB
-// table of silu results in shared memory, so one CTA per SM carries all their warps.
-constexpr int quant_threads(bool fp16, bool silu) {
-  return fp16 && silu ? 1024 : kThreads;
+// table of silu results in shared memory, so one CTA per SM carries all their warps.  The
+// bf16 masked silu instances also take one CTA of 24 warps per SM: a masked grid is sized
+// without knowing the live rows, and its CTAs that find no task cost less as a third as
+// many larger CTAs (decode batch without a hint: 4.07 -> 3.48 us; [32, 384, 2x4096] with
+// 6360 live rows: 24.42 -> 24.02 us).
+constexpr int quant_threads(bool fp16, bool silu, bool masked) {
+  return fp16 && silu ? 1024 : (silu && masked ? 768 : kThreads);
 }
 // Tasks a CTA of an instance takes in a call too small to fill the grid: one per warp,
-// except in the fp16 silu instances, whose large CTAs then deal consecutive tasks
-// round-robin over the grid and are given 8 each, so a small call spreads over four times
-// as many SMs (each SM's ingress from memory, not its warps, bounds such a call: a
-// [64, 2x2048] call takes 2.3 us instead of 3.6 us).
-constexpr int quant_small_tasks_per_cta(bool fp16, bool silu) {
-  return fp16 && silu ? 8 : quant_threads(fp16, silu) / 32;
+// except in the one-CTA-per-SM silu instances, whose large CTAs then deal consecutive tasks
+// round-robin over the grid and are given 8 each, so a small call spreads over as many SMs
+// as 8-warp CTAs would (each SM's ingress from memory, not its warps, bounds such a call:
+// a fp16 [64, 2x2048] call takes 2.3 us instead of 3.6 us).
+constexpr int quant_small_tasks_per_cta(bool fp16, bool silu, bool masked) {
+  return silu && (fp16 || masked) ? 8 : quant_threads(fp16, silu, masked) / 32;
 }
 constexpr int kMaxExperts = 4096;             // masked scheduler: E <= kMaxExperts
 constexpr int kBuckets = 256;                 // masked scheduler: row-to-expert buckets

@@ -68,9 +68,10 @@ struct Slot {
 // Tuning, per instance (compile-time), from sweeps on GB300: tasks per warp batch, whether
 // the next batch's loads are issued before the current batch is computed, and the CTAs per
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
-// CTAs/SM (64 registers).  bf16 silu, 3 CTAs/SM: flat one task pipelined, masked two tasks
-// loaded then computed.  fp16 silu: one CTA of quant_threads() per SM (its table fills most
-// of the shared memory), one task pipelined.
+// CTAs/SM (64 registers).  bf16 silu: flat one task pipelined at 3 CTAs/SM; masked two
+// tasks loaded then computed, one CTA of 24 warps per SM (80 registers).  fp16 silu: one
+// CTA of quant_threads() per SM (its table fills most of the shared memory), one task
+// pipelined.
 // The light flavour of the plain flat instances (kLight): one task per batch at 6 CTAs/SM
 // (40 registers, 48 warps per SM).  It ramps up faster when each warp has only a few
 // tasks, and the launcher takes it below about 8 tasks per warp of the standard grid
@@ -80,16 +81,16 @@ template <bool kFp16, bool kSilu, bool kMasked, bool kLight = false>
 struct Tuning {
   static_assert(!kLight || (!kSilu && !kMasked), "the light flavour is plain flat only");
   static constexpr bool f16_silu = kFp16 && kSilu;
-  static constexpr int threads = quant_threads(kFp16, kSilu);
+  static constexpr int threads = quant_threads(kFp16, kSilu, kMasked);
   // Tasks dealt round-robin over the CTAs (consecutive tasks to consecutive CTAs) instead
   // of in blocks of one per warp, in masked calls and in flat calls with fewer tasks than
   // warps: see quant_small_tasks_per_cta.  (Large flat calls keep the blocks: 14.8 us
   // against 15.2 us round-robin for fp16 silu [8192, 2x2048]; masked silu [32, 384,
   // 2x4096]: 22.9 us round-robin against 23.3 us.)
-  static constexpr bool round_robin = f16_silu;
+  static constexpr bool round_robin = f16_silu || (kSilu && kMasked);
   static constexpr int batch = (f16_silu || kLight || (kSilu && !kMasked)) ? 1 : 2;
   static constexpr bool pipeline = f16_silu || (kSilu && !kMasked);
-  static constexpr int min_blocks = f16_silu ? 1 : (kLight ? 6 : (!kSilu ? 4 : 3));
+  static constexpr int min_blocks = (f16_silu || (kSilu && kMasked)) ? 1 : (kLight ? 6 : (!kSilu ? 4 : 3));
 };
 
 // kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32, 3 fp32 scales with
@@ -120,6 +121,58 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
     else copy_to_smem_async<kT>(smem, kSiluBf16, kSiluBf16Words / 4);
   }
 
+  // The rows of this warp's first batch go to L2 before the dependency wait.  A prefetch
+  // reads no value into the kernel and L2 is the point of coherence for device memory, so
+  // whatever the previous kernel writes to x, the loads after the wait see it; when x was
+  // not written by that kernel, the first DRAM round trip of this call overlaps its tail
+  // (back-to-back calls on independent buffers, benchmarked workload: 14.95 -> 14.27 us;
+  // fused silu [8192, 2x2048]: 15.01 -> 14.29 us; [64, 4096]: 1.88 -> 1.51 us).
+  //   flat  : the exact tasks of the first batch (the first task and the batch's strides).
+  //   masked: with a hint of the live rows per expert, the rows of the first task guessed
+  //           as if every expert had exactly rows_hint live rows (hinted decode batch, bf16
+  //           silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us).  The guess only decides
+  //           what is prefetched: rows below rows_hint <= rows of experts below n, so every
+  //           prefetched address lies inside x.  Calls without a hint prefetch nothing: a
+  //           guess of one row per expert gained 0.08 us on the unhinted decode batch but
+  //           cost 0.15-0.18 us on the large masked silu calls.
+  {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t lu_log2 = p.lg_log2 + p.ug_log2;
+    const uint32_t local = lane & ((1u << lu_log2) - 1u);
+    const uint32_t kk0 = local & ((1u << p.lg_log2) - 1u);
+    auto prefetch_row = [&](int64_t grow, uint32_t g) {
+      const uint16_t* src = static_cast<const uint16_t*>(p.x) + grow * p.in_row +
+                            (static_cast<int64_t>(g) << (4u + p.lg_log2)) + kk0 * 16u;
+      prefetch_l2(src);
+      if constexpr (kSilu) prefetch_l2(src + p.hidden);
+    };
+    if constexpr (kMasked) {
+      if (p.rows_hint > 0u) {
+        const uint32_t u = (first_task(Tune::round_robin) << (5u - lu_log2)) + (lane >> lu_log2);
+        const uint32_t R = udiv(u, p.upr, p.upr_magic);
+        const uint32_t e = udiv(R, p.rows_hint, p.rows_hint_magic);
+        const uint32_t g = ((u - R * p.upr) << p.ug_log2) + (local >> p.lg_log2);
+        if (e < p.n && g < p.ng)
+          prefetch_row(static_cast<int64_t>(e) * p.rows + (R - e * p.rows_hint), g);
+      }
+    } else {
+      const uint32_t upw_log2 = 5u - lu_log2;
+      const uint32_t tasks = (p.units_flat + (1u << upw_log2) - 1u) >> upw_log2;
+      const uint32_t stride = gridDim.x * kW;
+      const uint32_t t0 = first_task(Tune::round_robin && tasks < stride);
+      const int nb = (kB > 1 && tasks <= stride) ? 1 : kB;
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const uint32_t u = ((t0 + b * stride) << upw_log2) + (lane >> lu_log2);
+        if (b < nb && u < p.units_flat) {
+          const uint32_t R = udiv(u, p.upr, p.upr_magic);
+          const uint32_t g = ((u - R * p.upr) << p.ug_log2) + (local >> p.lg_log2);
+          if (g < p.ng) prefetch_row(R, g);
+        }
+      }
+    }
+  }
+
   griddep_wait();
   griddep_launch_dependents();
 
@@ -127,32 +180,6 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
   int32_t* bucket = prefix + (p.n + 1);
   uint32_t bshift = 0u;
   if constexpr (kMasked) {
-    // With a hint of the live rows per expert, the rows of this warp's first task, guessed
-    // as if every expert had exactly rows_hint live rows, go to L2 while masked_m is read
-    // (hinted decode batch, bf16 silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us).  Calls
-    // without a hint prefetch nothing: a guess of one row per expert gained 0.08 us on the
-    // unhinted decode batch but cost 0.15-0.18 us on the large masked silu calls.
-    // The guess only decides what is prefetched: rows below rows_hint <= rows of experts
-    // below n, so every prefetched address lies inside x.
-    if (p.rows_hint > 0u) {
-      const uint32_t lane = threadIdx.x & 31u;
-      const uint32_t lu_log2 = p.lg_log2 + p.ug_log2;
-      const uint32_t local = lane & ((1u << lu_log2) - 1u);
-      const uint32_t u = (first_task(Tune::round_robin) << (5u - lu_log2)) +
-                         (lane >> lu_log2);
-      const uint32_t R = udiv(u, p.upr, p.upr_magic);
-      const uint32_t e = udiv(R, p.rows_hint, p.rows_hint_magic);
-      const uint32_t g = ((u - R * p.upr) << p.ug_log2) + (local >> p.lg_log2);
-      if (e < p.n && g < p.ng) {
-        const uint32_t row = R - e * p.rows_hint;
-        const uint16_t* src = static_cast<const uint16_t*>(p.x) +
-                              (static_cast<int64_t>(e) * p.rows + row) * p.in_row +
-                              (static_cast<int64_t>(g) << (4u + p.lg_log2)) +
-                              (local & ((1u << p.lg_log2) - 1u)) * 16u;
-        prefetch_l2(src);
-        if constexpr (kSilu) prefetch_l2(src + p.hidden);
-      }
-    }
     masked_prefix<kT>(p.masked_m, p.n, p.rows, prefix);
     __syncthreads();
     // A grid sized without knowing the live counts (no hint) often has CTAs with no task:

@@ -92,7 +92,7 @@ def test_hint_prefetch_stays_inside_x():
     x = [E, tokens_pad, H_in]."""
     for E, rows, H, G, packed, silu, hint, rr in itertools.product(
             [1, 3, 32], [1, 5, 40], [128, 384, 2048], [16, 32, 64, 128], [0, 1], [0, 1],
-            [1, 3, 7, 1000], [0, 1]):
+            [1, 3, 7, 1000], [0, 24, 32]):
         if H % G:
             continue
         lg_log2 = {16: 0, 32: 1, 64: 2, 128: 3}[G]
@@ -104,7 +104,7 @@ def test_hint_prefetch_stays_inside_x():
         upr_magic = 0xFFFFFFFF if upr == 1 else (1 << 32) // upr
         hint_magic = 0xFFFFFFFF if rows_hint <= 1 else (1 << 32) // rows_hint
         lu = lg_log2 + ug_log2
-        grid, warps = 6, 32 if rr else 8
+        grid, warps = 6, rr if rr else 8
         b, w, lane = np.meshgrid(np.arange(grid), np.arange(warps), np.arange(32), indexing="ij")
         b, w, lane = b.ravel().astype(np.int64), w.ravel().astype(np.int64), lane.ravel()
         first = b + grid * w if rr else b * warps + w
@@ -172,3 +172,43 @@ def test_requant_chunks_stay_inside_and_cover_every_live_row_once():
                                        for ee in range(E) for rr in range(int(live[ee]))] or
                                       [np.zeros(0, np.int64)]))
         assert np.array_equal(got, want), (E, m, k, G, V)
+
+
+def test_flat_first_batch_prefetch_stays_inside_x():
+    """ptgq_kernel.cuh: before the dependency wait every flat warp prefetches its first
+    batch (the first task and, with two-task batches, the task a grid stride further): units
+    below the call's units, groups below the row's groups.  Over shapes, group sizes, scale
+    formats, silu, batch sizes, both dealings and grids larger and smaller than the work,
+    every prefetched chunk (gate and, with silu, up) lies inside x = [T, H_in]."""
+    for T, H, G, packed, silu, kB, rr, grid in itertools.product(
+            [1, 7, 64, 333], [128, 384, 2048], [16, 32, 64, 128], [0, 1], [0, 1], [1, 2],
+            [0, 1], [1, 6, 600]):
+        if H % G:
+            continue
+        lg_log2 = {16: 0, 32: 1, 64: 2, 128: 3}[G]
+        ug_log2 = 2 if packed else 0
+        ng = H // G
+        upr = (ng + (1 << ug_log2) - 1) >> ug_log2
+        in_row = 2 * H if silu else H
+        units = T * upr
+        lu = lg_log2 + ug_log2
+        upw_log2 = 5 - lu
+        tasks = (units + (1 << upw_log2) - 1) >> upw_log2
+        warps = 32 if rr else 8
+        stride = grid * warps
+        b, w, lane = np.meshgrid(np.arange(grid), np.arange(warps), np.arange(32), indexing="ij")
+        b, w, lane = b.ravel().astype(np.int64), w.ravel().astype(np.int64), lane.ravel()
+        use_rr = rr and tasks < stride
+        t0 = b + grid * w if use_rr else b * warps + w
+        nb = 1 if (kB > 1 and tasks <= stride) else kB
+        local = lane & ((1 << lu) - 1)
+        for bb in range(nb):
+            u = ((t0 + bb * stride) << upw_log2) + (lane >> lu)
+            ok = u < units
+            R = _udiv(u, upr, 0xFFFFFFFF if upr == 1 else (1 << 32) // upr)
+            assert np.array_equal(R[ok], (u // upr)[ok])
+            g = ((u - R * upr) << ug_log2) + (local >> lg_log2)
+            ok &= g < ng
+            off = R * in_row + (g << (4 + lg_log2)) + (local & ((1 << lg_log2) - 1)) * 16
+            end = off + (H if silu else 0) + 16
+            assert np.all(R[ok] < T) and np.all(end[ok] <= T * in_row)
