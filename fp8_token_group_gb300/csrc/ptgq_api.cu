@@ -251,6 +251,7 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   if (!masked && !fuse_silu && !key.light && tasks > 16 * full * kWarps) {
     want = (tasks + per_cta * 8 - 1) / (per_cta * 8);
     full = want;
+    p.prefetch_next = 1u;
   }
   if (!masked) {
     const int64_t zero_chunks = (p.zero_q_end - p.zero_q_begin) / 16 + p.zero_s_rows * g.ncol;

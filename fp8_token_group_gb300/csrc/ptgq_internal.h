@@ -62,6 +62,7 @@ struct Params {
   uint32_t rows_hint;        // masked: the caller's expected live rows per expert,
                              // min(expected_m, rows); 0 without a hint
   uint32_t rows_hint_magic;  // floor(2^32 / rows_hint), or 0xFFFFFFFF when rows_hint <= 1
+  uint32_t prefetch_next;    // plain flat calls on several waves: 1 to prefetch the next batch
   // Flat zero-fill of padding (rows [T, rows) of q; scale rows past T).
   int64_t zero_q_begin;      // byte offsets into q, multiples of 16
   int64_t zero_q_end;

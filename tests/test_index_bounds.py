@@ -212,3 +212,50 @@ def test_flat_first_batch_prefetch_stays_inside_x():
             off = R * in_row + (g << (4 + lg_log2)) + (local & ((1 << lg_log2) - 1)) * 16
             end = off + (H if silu else 0) + 16
             assert np.all(R[ok] < T) and np.all(end[ok] <= T * in_row)
+
+
+def test_flat_next_batch_prefetch_stays_inside_x():
+    """ptgq_kernel.cuh: on a grid of several waves (plain flat calls with p.prefetch_next),
+    each batch of KB tasks starting at task t prefetches the chunks of tasks t + (KB + i) *
+    stride, i < KB, computed in 64 bits: units below the call's units, groups below the row's
+    groups.  Over shapes, group sizes, scale formats, batch sizes and grids of one wave down to
+    grids that leave 8 or more tasks per warp, for every batch every warp runs, every
+    prefetched chunk lies inside x = [T, H] and is the chunk that task's load reads."""
+    for T, H, G, packed, kB, grid in itertools.product(
+            [7, 333, 1031], [128, 384, 2048], [16, 32, 64, 128], [0, 1], [1, 2], [1, 3, 40]):
+        if H % G:
+            continue
+        lg_log2 = {16: 0, 32: 1, 64: 2, 128: 3}[G]
+        ug_log2 = 2 if packed else 0
+        ng = H // G
+        upr = (ng + (1 << ug_log2) - 1) >> ug_log2
+        units = T * upr
+        lu = lg_log2 + ug_log2
+        upw_log2 = 5 - lu
+        tasks = (units + (1 << upw_log2) - 1) >> upw_log2
+        warps = 8
+        stride = grid * warps
+        if tasks <= stride:
+            continue                      # one-task batches without the prefetch
+        b, w, lane = np.meshgrid(np.arange(grid), np.arange(warps), np.arange(32), indexing="ij")
+        b, w, lane = b.ravel().astype(np.int64), w.ravel().astype(np.int64), lane.ravel()
+        first = b * warps + w
+        local = lane & ((1 << lu) - 1)
+        gj = local >> lg_log2
+        kk = local & ((1 << lg_log2) - 1)
+        magic = 0xFFFFFFFF if upr == 1 else (1 << 32) // upr
+        t = first.copy()
+        while np.any(t < tasks):
+            live = t < tasks
+            for i in range(kB):
+                tn = t + (kB + i) * stride
+                un = (tn << upw_log2) + (lane >> lu)
+                ok = live & (un < units)
+                R = _udiv(np.where(ok, un, 0), upr, magic)
+                assert np.array_equal(R[ok], (un // upr)[ok])
+                g = ((un - R * upr) << ug_log2) + gj
+                ok &= g < ng
+                off = R * H + g * G + kk * 16
+                assert np.all(R[ok] < T) and np.all(off[ok] + 16 <= T * H)
+                assert np.array_equal(off[ok], ((un // upr) * H + g * G + kk * 16)[ok])
+            t = t + kB * stride
