@@ -220,7 +220,9 @@ int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens, int64_t h
  *   x_scale       device float per-token-group scales; element (e, r, g) at
  *                 e * scale_stride_e + r * scale_stride_m + g * scale_stride_g (strides in
  *                 elements, e.g. the column-major [E, m, k/group] layout of the page:
- *                 (m * k/group, 1, m)).  The caller guarantees every index is inside it.
+ *                 (m * k/group, 1, m)).  The caller guarantees that every element with
+ *                 e < num_experts, r < m and g < k/group lies inside it, dead rows included
+ *                 (the kernel may prefetch their scales into L2).
  *   masked_m      device int32[num_experts] live rows per expert, or NULL.
  *   output_scale  device pointer to the one binary32 per-tensor output scale.
  *   out           device e4m3 codes [num_experts, m, k], 16-byte aligned.

@@ -174,6 +174,32 @@ def test_requant_chunks_stay_inside_and_cover_every_live_row_once():
         assert np.array_equal(got, want), (E, m, k, G, V)
 
 
+def test_requant_speculative_prefetch_stays_inside_x_and_x_scale():
+    """ptgq_next.cu, requant_kernel: before the dependency wait each lane prefetches its
+    chunk of the warp's first task as if every row were live (c0 = warp * 32 + lane, with
+    the slot and row from the same 32-bit divisions as the loop), and that chunk's group
+    scale.  Over shapes, group sizes, chunk widths and grids: whenever r0 < m, the code
+    chunk lies inside x = [E, m, k] and the scale index inside the [E, m, k/G] grid."""
+    for E, m, k, G, V, grid_ctas in itertools.product(
+            [1, 3, 8, 33], [1, 5, 64, 1024], [16, 48, 128, 3584], [16, 32, 64, 128], [16, 32],
+            [1, 7, 456]):
+        if k % G or k % V:
+            continue
+        cpr = k // V
+        c0 = np.arange(grid_ctas * 8 * 32, dtype=np.int64)
+        S0 = _udiv(c0, cpr, _magic(cpr))
+        assert np.array_equal(S0, c0 // cpr)
+        r0 = _udiv(S0, E, _magic(E))
+        assert np.array_equal(r0, S0 // E)
+        ok = r0 < m
+        e0 = S0 - r0 * E
+        col0 = c0 - S0 * cpr
+        off = (e0 * m + r0) * k + col0 * V
+        assert np.all(e0[ok] < E) and np.all(off[ok] >= 0) and np.all(off[ok] + V <= E * m * k)
+        g0 = (col0 * V) >> int(np.log2(G))
+        assert np.all(g0[ok] < k // G)
+
+
 def test_flat_first_batch_prefetch_stays_inside_x():
     """ptgq_kernel.cuh: before the dependency wait every flat warp prefetches its first
     batch (the first task and, with two-task batches, the task a grid stride further): units
