@@ -378,6 +378,38 @@ def test_masked_all_empty_and_zero_experts():
     assert gq.size == 0 and gs.size == 0
 
 
+@pytest.mark.parametrize("E", [1, 2, 31, 32, 33])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("silu", [False, True])
+@pytest.mark.parametrize("size", ["decode", "large"])
+def test_masked_expert_lookup_around_32_experts(E, dt, silu, size):
+    """Masked calls of at most 32 experts scan masked_m per warp; decode-sized ones (at most
+    one task per warp) look the expert up by shuffles, larger ones through the shared-memory
+    buckets, and more than 32 experts take the block-wide prefix.  Short rows (H = 128 at
+    G = 128: four rows per warp task; H = 256 at G = 16 packed: two) make tasks cross experts,
+    with empty experts, negative counts and counts past the pad in between."""
+    rng = np.random.default_rng(E * 10 + silu + (size == "large") * 100)
+    if size == "decode":
+        rows = 8
+        mm = rng.integers(0, 3, E)
+    else:
+        rows = max(8, 32768 // E)
+        mm = rng.integers(rows // 2, rows + 4, E)
+    mm[rng.random(E) < 0.2] = 0
+    if E > 2:
+        mm[1] = -4
+        mm[2] = rows + 9
+    mm = mm.astype(np.int32)
+    for H, c in [(128, Case(silu=silu)),
+                 (256, Case(group=16, silu=silu, scale_fmt=P.SCALE_UE8M0_PACKED,
+                            layout=P.COL_MAJOR_TMA))]:
+        x = synth.sweep_input(E + 7, E * rows, 2 * H if silu else H, dt).reshape(E, rows, -1)
+        compare(x, c, masked_m=mm)
+        if size == "decode":
+            c.expected_m = 1
+            compare(x, c, masked_m=mm)
+
+
 def test_many_experts():
     E = 1000
     x = synth.normal((E, 4, 256), torch.bfloat16, seed=2)

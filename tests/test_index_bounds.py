@@ -285,3 +285,37 @@ def test_flat_next_batch_prefetch_stays_inside_x():
                 assert np.all(R[ok] < T) and np.all(off[ok] + 16 <= T * H)
                 assert np.array_equal(off[ok], ((un // upr) * H + g * G + kk * 16)[ok])
             t = t + kB * stride
+
+
+def test_masked_warp_lookup_finds_the_owner_of_every_live_row():
+    """ptgq_kernel.cuh, masked calls of at most 32 experts: each warp scans the clamped
+    masked_m with shuffles (w_key[e] = exclusive prefix for e < n, all ones past n), and a
+    lane with live row R takes the largest e with w_key[e] <= R by a five-step search over
+    lanes lo + 16, 8, 4, 2, 1.  Over expert counts 1..32 and live counts with empty experts,
+    negatives and counts past the pad: the search reads lanes 0..31 only, and for every live
+    row R it returns the expert that owns R and the row R - w_key[e] < masked_m[e]."""
+    rng = np.random.default_rng(11)
+    for n in range(1, 33):
+        for rows in [1, 3, 384]:
+            for _ in range(20):
+                mm = rng.integers(-3, rows + 4, n)
+                mm[rng.random(n) < 0.3] = 0
+                c = np.clip(mm, 0, rows).astype(np.int64)
+                incl = np.cumsum(c)
+                key = np.full(32, 0xFFFFFFFF, np.int64)
+                key[:n] = incl - c
+                live = int(incl[-1])
+                R = np.arange(live, dtype=np.int64)
+                lo = np.zeros(live, np.int64)
+                base = np.zeros(live, np.int64)
+                for step in [16, 8, 4, 2, 1]:
+                    src = lo + step
+                    assert src.max(initial=0) <= 31
+                    v = key[src]
+                    take = v <= R
+                    lo = np.where(take, src, lo)
+                    base = np.where(take, v, base)
+                owner = np.repeat(np.arange(n), c)
+                assert np.array_equal(lo, owner)
+                assert np.array_equal(R - base, R - (incl - c)[owner])
+                assert np.all(R - base < c[owner])
