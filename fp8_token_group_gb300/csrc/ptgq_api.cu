@@ -23,10 +23,14 @@ const void* kernel_for_fp16_flat(int int8, int fmt, int silu);
 const void* kernel_for_fp16_masked(int int8, int fmt, int silu);
 const void* kernel_for_bf16_flat_light(int int8, int fmt);
 const void* kernel_for_fp16_flat_light(int int8, int fmt);
+const void* kernel_for_bf16_flat_light_pf(int int8, int fmt);
+const void* kernel_for_fp16_flat_light_pf(int int8, int fmt);
 int table_bytes_bf16(int silu);
 int table_bytes_fp16(int silu);
 
 const void* kernel_for(const KernelKey& k) {
+  if (k.light == 2 && !k.masked && !k.silu)
+    return k.fp16 ? kernel_for_fp16_flat_light_pf(k.int8, k.fmt) : kernel_for_bf16_flat_light_pf(k.int8, k.fmt);
   if (k.light && !k.masked && !k.silu)
     return k.fp16 ? kernel_for_fp16_flat_light(k.int8, k.fmt) : kernel_for_bf16_flat_light(k.int8, k.fmt);
   if (k.fp16)
@@ -237,6 +241,13 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
     fn = kernel_for(key);
     rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
     if (rc != PTGQ_OK) return rc;
+    if (tasks > static_cast<int64_t>(per_sm) * sms * kWarps) {
+      key.light = 2;
+      p.prefetch_next = 1u;
+      fn = kernel_for(key);
+      rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
+      if (rc != PTGQ_OK) return rc;
+    }
   }
   const int per_cta = quant_small_tasks_per_cta(key.fp16 != 0, key.silu != 0, key.masked != 0);
   int64_t want = (tasks + per_cta - 1) / per_cta;

@@ -40,6 +40,20 @@ const void* kernel_for_bf16_flat_light(int int8, int fmt) {
   return table[(int8 ? 4 : 0) + fmt];
 }
 
+const void* kernel_for_bf16_flat_light_pf(int int8, int fmt) {
+  static const void* const table[8] = {
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 0, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 1, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 2, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 3, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 0, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 1, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 2, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<false, true, 3, false, false, 2>),
+  };
+  return table[(int8 ? 4 : 0) + fmt];
+}
+
 int table_bytes_bf16(int silu) { return silu ? SmemTables<false, true>::bytes : 0; }
 
 }  // namespace ptgq

@@ -40,6 +40,20 @@ const void* kernel_for_fp16_flat_light(int int8, int fmt) {
   return table[(int8 ? 4 : 0) + fmt];
 }
 
+const void* kernel_for_fp16_flat_light_pf(int int8, int fmt) {
+  static const void* const table[8] = {
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 0, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 1, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 2, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<true, false, 3, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 0, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 1, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 2, false, false, 2>),
+      reinterpret_cast<const void*>(&quant_kernel<true, true, 3, false, false, 2>),
+  };
+  return table[(int8 ? 4 : 0) + fmt];
+}
+
 int table_bytes_fp16(int silu) { return silu ? SmemTables<true, true>::bytes : 0; }
 
 }  // namespace ptgq

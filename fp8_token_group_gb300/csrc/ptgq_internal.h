@@ -76,7 +76,8 @@ struct KernelKey {
   int fmt;        // 0 fp32, 1 UE8M0 packed, 2 UE8M0 as fp32, 3 fp32 with approximate division
   int silu;       // fused silu(gate) * up
   int masked;     // masked (EP-MoE) scheduler (else flat)
-  int light;      // plain flat only: the flavour for a few tasks per warp
+  int light;      // plain flat only: 1 the flavour for a few tasks per warp, 2 the same with
+                  // the next-batch prefetch (more than one task per warp)
 };
 
 // Returns the __global__ function of an instance (defined in the instance TUs).

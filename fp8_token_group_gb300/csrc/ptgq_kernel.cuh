@@ -96,15 +96,15 @@ struct Tuning {
 // kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32, 3 fp32 scales with
 // the element quotients taken by approximate division (fast-math interop).  The scale
 // format is a template parameter so that only the packed instances carry the exponent OR.
-template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked, bool kLight = false>
-__global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::threads),
-                                  (Tuning<kFp16, kSilu, kMasked, kLight>::min_blocks))
+template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked, int kLight = 0>
+__global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::threads),
+                                  (Tuning<kFp16, kSilu, kMasked, kLight != 0>::min_blocks))
     quant_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr bool kPow2 = kFmt == 1 || kFmt == 2;
   constexpr bool packed = kFmt == 1;
   using Tab = SmemTables<kFp16, kSilu>;
-  using Tune = Tuning<kFp16, kSilu, kMasked, kLight>;
+  using Tune = Tuning<kFp16, kSilu, kMasked, kLight != 0>;
   constexpr int kB = Tune::batch;
   constexpr int kT = Tune::threads;
   constexpr int kW = kT / 32;
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
       Raw16 ca[KB], cb[KB];
 #pragma unroll
       for (int i = 0; i < KB; ++i) issue(std::false_type{}, t + i * stride, cur[i], ca[i], cb[i]);
-      if constexpr (PF && !kMasked && !kLight) {
+      if constexpr (PF && !kMasked && kLight != 1) {
 #pragma unroll
         for (int i = 0; i < KB; ++i) {
           const uint64_t tn = t + static_cast<uint64_t>(KB + i) * stride;
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight>::thread
     // When no warp has a second task (small or decode-sized work), one-task batches: the
     // empty slots of a wider batch would still be computed and only lengthen the call.
     if (kB > 1 && total_tasks <= stride) batches(one, no);
-    else if (!kMasked && !kLight && p.prefetch_next) batches(wide, yes);
+    else if (!kMasked && kLight != 1 && p.prefetch_next) batches(wide, yes);
     else batches(wide, no);
   } else {
     pipelined();
