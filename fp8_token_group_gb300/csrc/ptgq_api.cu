@@ -24,11 +24,20 @@ const void* kernel_for_fp16_masked(int int8, int fmt, int silu);
 const void* kernel_for_bf16_flat_light(int int8, int fmt);
 const void* kernel_for_fp16_flat_light(int int8, int fmt);
 const void* kernel_for_bf16_flat_light_pf(int int8, int fmt);
+const void* kernel_for_bf16_flat_checked(int fmt, int silu);
+const void* kernel_for_bf16_masked_checked(int fmt, int silu);
+const void* kernel_for_fp16_flat_checked(int fmt, int silu);
+const void* kernel_for_fp16_masked_checked(int fmt, int silu);
 const void* kernel_for_fp16_flat_light_pf(int int8, int fmt);
 int table_bytes_bf16(int silu);
 int table_bytes_fp16(int silu);
 
 const void* kernel_for(const KernelKey& k) {
+  if (k.checked && !k.int8 && k.fmt != 3) {
+    if (k.fp16)
+      return k.masked ? kernel_for_fp16_masked_checked(k.fmt, k.silu) : kernel_for_fp16_flat_checked(k.fmt, k.silu);
+    return k.masked ? kernel_for_bf16_masked_checked(k.fmt, k.silu) : kernel_for_bf16_flat_checked(k.fmt, k.silu);
+  }
   if (k.light == 2 && !k.masked && !k.silu)
     return k.fp16 ? kernel_for_fp16_flat_light_pf(k.int8, k.fmt) : kernel_for_bf16_flat_light_pf(k.int8, k.fmt);
   if (k.light && !k.masked && !k.silu)
@@ -218,7 +227,7 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
 
   // Internal format 3: fp32 scales with approximate element division (fast-math interop).
   const int kfmt = (scale_fmt == PTGQ_SCALE_FP32 && (flags & PTGQ_FLAG_FAST_DIVIDE)) ? 3 : scale_fmt;
-  KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, kfmt, fuse_silu, masked, 0};
+  KernelKey key{dtype == PTGQ_FP16, out_dtype == PTGQ_INT8, kfmt, fuse_silu, masked, 0, eps < kExactAmaxEps};
   const void* fn = kernel_for(key);
   const size_t smem = dynamic_smem_bytes(key, masked ? n : 0);
   int dev = 0;
@@ -236,7 +245,7 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
   const int64_t tasks = (units_max * lanes_per_unit + 31) / 32;
   // Plain flat work of at most about 8 tasks per warp of the standard grid: the light
   // flavour (one task per batch, more warps per SM) ramps up faster.
-  if (!masked && !fuse_silu && tasks <= 8 * static_cast<int64_t>(per_sm) * sms * kWarps) {
+  if (!masked && !fuse_silu && !key.checked && tasks <= 8 * static_cast<int64_t>(per_sm) * sms * kWarps) {
     key.light = 1;
     fn = kernel_for(key);
     rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);

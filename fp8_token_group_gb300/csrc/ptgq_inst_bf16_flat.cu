@@ -56,4 +56,18 @@ const void* kernel_for_bf16_flat_light_pf(int int8, int fmt) {
 
 int table_bytes_bf16(int silu) { return silu ? SmemTables<false, true>::bytes : 0; }
 
+// e4m3 instances that vote on the amax range (eps below the fast arithmetic's range);
+// fmt 0..2 (the fast-divide and int8 instances always vote).
+const void* kernel_for_bf16_flat_checked(int fmt, int silu) {
+  static const void* const table[6] = {
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 0, false, false, 0, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 0, true, false, 0, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 1, false, false, 0, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 1, true, false, 0, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 2, false, false, 0, true>),
+      reinterpret_cast<const void*>(&quant_kernel<false, false, 2, true, false, 0, true>),
+  };
+  return table[fmt * 2 + (silu ? 1 : 0)];
+}
+
 }  // namespace ptgq

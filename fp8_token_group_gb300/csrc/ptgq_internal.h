@@ -78,7 +78,14 @@ struct KernelKey {
   int masked;     // masked (EP-MoE) scheduler (else flat)
   int light;      // plain flat only: 1 the flavour for a few tasks per warp, 2 the same with
                   // the next-batch prefetch (more than one task per warp)
+  int checked;    // e4m3, fmt 0..2: the instances that vote on the amax range (eps below
+                  // kExactAmaxEps)
 };
+
+// Lower end of the amax range over which the kernels' fast scale and quotient arithmetic is
+// exact (the same bound as kExactAmaxMin in ptgq_kernel.cuh): calls with a smaller eps take
+// the checked instances.
+constexpr float kExactAmaxEps = 1e-24f;
 
 // Returns the __global__ function of an instance (defined in the instance TUs).
 const void* kernel_for(const KernelKey& k);

@@ -35,7 +35,9 @@ namespace ptgq {
 constexpr int kSiluF16Words = (PTGQ_SILU_F16_ENTRIES + 3) / 4 * 4;
 constexpr int kSiluBf16Words = 2 * PTGQ_SILU_BF16_SPAN;
 // Range of amax over which the fast scale and quotient arithmetic is proven exact (checked
-// for every pair of 16-bit values and 1.3e9 sampled binary32 pairs down to this amax).
+// for every pair of 16-bit values and 1.3e9 sampled binary32 pairs down to this amax).  The
+// launcher takes the checked instances (kChecked) when eps is below it; ptgq_api.cu holds
+// the same bound.
 constexpr float kExactAmaxMin = 1e-24f;
 constexpr float kFltMax = 3.40282346638528859812e+38f;
 
@@ -96,7 +98,12 @@ struct Tuning {
 // kFmt: 0 fp32 scales, 1 UE8M0 packed four per int32, 2 UE8M0 as fp32, 3 fp32 scales with
 // the element quotients taken by approximate division (fast-math interop).  The scale
 // format is a template parameter so that only the packed instances carry the exponent OR.
-template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked, int kLight = 0>
+// kChecked: every warp votes on whether all its groups' amax lie in [kExactAmaxMin, FLT_MAX]
+// and otherwise takes IEEE division (below).  Needed when eps < kExactAmaxMin; the int8
+// instances always vote, since a NaN quotient (an infinite element of a group whose amax is
+// infinite) has no integer code without a select per element.
+template <bool kFp16, bool kInt8, int kFmt, bool kSilu, bool kMasked, int kLight = 0,
+          bool kChecked = false>
 __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::threads),
                                   (Tuning<kFp16, kSilu, kMasked, kLight != 0>::min_blocks))
     quant_kernel(const Params p) {
@@ -385,16 +392,23 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
     uint64_t y[8];
     // The scale and quotients below (constant reciprocal with one correction, reciprocal
     // with an exact residual) give the IEEE results for kExactAmaxMin <= amax <= FLT_MAX.
-    // A warp with any group outside that range -- a tiny eps over an all-zero group, tiny
-    // data, or an infinite amax from an infinite element or a silu product that overflows
-    // binary32 -- takes IEEE division for the scale and every quotient instead (uniform
-    // branch; real activations never reach it).
-    if (__all_sync(0xFFFFFFFFu, amax >= kExactAmaxMin && amax <= kFltMax)) {
+    // amax >= eps, so only an infinite amax (an infinite element, or a silu product that
+    // overflows binary32) lies outside that range unless eps < kExactAmaxMin.  The e4m3
+    // instances handle it with three selects: s = +inf, and the quotients v / +inf formed
+    // as v * 0 (UE8M0: the inverse of 2^128 taken as 0) or through the residual step with
+    // r = 1/s = 0 and -s taken as 0: +-0 for finite v, NaN (0x7F) for infinite v.  The
+    // checked, int8 and fast-divide instances vote instead: a warp with any group outside
+    // the range takes IEEE division for the scale and every quotient (uniform branch).  The
+    // vote and its branch cost 1-4% (sweep [32768, 7168] G = 128: 103.1 against 99.3 us
+    // with the selects; masked silu fp16: 23.24 against 22.53 us).
+    constexpr bool kVote = kInt8 || kChecked || kFmt == 3;
+    if (!kVote || __all_sync(0xFFFFFFFFu, amax >= kExactAmaxMin && amax <= kFltMax)) {
       s = div_by_const(amax, p.fmax, rfmax);
+      if constexpr (!kVote) s = amax > kFltMax ? amax : s;     // the quotient is NaN for +inf
       if constexpr (kPow2) {
         s = fmaxf(s, p.scale_floor);
         e = ue8m0_exponent(s);
-        const float inv = ue8m0_inverse(e);
+        const float inv = (!kVote && e == 255u) ? 0.0f : ue8m0_inverse(e);
         const uint64_t inv2 = pk2(inv, inv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) y[i] = mul2(v[i], inv2);
@@ -407,7 +421,8 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
         }
       } else {
         const float r = __frcp_rn(s);
-        const uint64_t r2 = pk2(r, r), ns2 = pk2(-s, -s);
+        const float ns = (!kVote && s > kFltMax) ? 0.0f : -s;
+        const uint64_t r2 = pk2(r, r), ns2 = pk2(ns, ns);
 #pragma unroll
         for (int i = 0; i < 8; ++i) y[i] = div2_by_scale(v[i], r2, ns2);
       }

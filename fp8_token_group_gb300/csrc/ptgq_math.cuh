@@ -90,7 +90,8 @@ PTGQ_HD uint32_t ue8m0_exponent(float s) {
 
 // 2^(127 - e), the exact reciprocal of the UE8M0 scale 2^(e - 127), for 1 <= e <= 254.
 // (e = 255 comes only from an infinite amax, whose scale 2^128 is +inf in binary32; the
-// kernel handles such groups by IEEE division instead.)
+// kernel multiplies such groups by 0 instead, which equals v / +inf for every v, or takes
+// IEEE division.)
 PTGQ_HD float ue8m0_inverse(uint32_t e) { return u2f((254u - e) << 23); }
 
 }  // namespace ptgq

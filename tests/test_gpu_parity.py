@@ -339,6 +339,43 @@ def test_nonfinite_amax_fixture_and_overflowing_silu(fmt):
                     masked_m=np.array([16, 3, 0, 9], np.int32))
 
 
+@pytest.mark.parametrize("T,H", [(64, 2048), (4096, 2048), (8192, 4096), (16384, 4096)])
+@pytest.mark.parametrize("fmt", [P.SCALE_FP32, P.SCALE_UE8M0_PACKED])
+def test_nonfinite_and_tiny_eps_on_every_flat_flavour(T, H, fmt):
+    """The plain flat launch shapes (light, light with the next-batch prefetch, one
+    persistent wave, several waves): groups with an infinite element (amax = +inf, handled
+    by selects in the e4m3 instances and by the warp vote in the int8 ones), and the same
+    input with eps = 1e-30 over zeroed groups (the checked instances)."""
+    g = torch.Generator().manual_seed(T + H)
+    x = torch.randn((T, H), generator=g)
+    n = max(8, T // 64)
+    x[torch.randint(0, T, (n,), generator=g), torch.randint(0, H, (n,), generator=g)] = float("inf")
+    x[1, 3] = -float("inf")
+    x[2, :256] = 0.0
+    x = x.to(torch.bfloat16)
+    for out in (P.E4M3, P.INT8):
+        compare(x, Case(scale_fmt=fmt, out_dtype=out, layout=P.COL_MAJOR_TMA))
+    xz = x.clone()
+    xz[torch.isinf(xz)] = 0.0
+    xz[5, 128:512] = 1e-30
+    compare(xz, Case(scale_fmt=fmt, eps=1e-30, layout=P.COL_MAJOR_TMA))
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("silu", [False, True])
+def test_tiny_eps_masked(dt, silu):
+    """eps below 1e-24 in masked calls (the checked masked instances), decode-sized and
+    larger, with all-zero and tiny groups among ordinary ones."""
+    for E, rows, mm in [(32, 8, [1] * 32), (8, 512, [512, 3, 0, 200, 511, 77, 1, 300])]:
+        H = 1024
+        x = synth.sweep_input(E + rows, E * rows, 2 * H if silu else H, dt).reshape(E, rows, -1)
+        x[0, 0, :128] = 0
+        x[3, 0, 128:256] = 1e-30 if dt == torch.bfloat16 else 0
+        for fmt in (P.SCALE_FP32, P.SCALE_UE8M0_PACKED):
+            compare(x, Case(eps=2.0 ** -140, scale_fmt=fmt, silu=silu),
+                    masked_m=np.array(mm, np.int32))
+
+
 def test_extreme_values():
     dt = torch.bfloat16
     x = torch.zeros((8, 256), dtype=dt)
