@@ -119,9 +119,10 @@ enum {
  *   fuse_silu       1: v = silu(gate) * up computed in binary32 before quantization.
  *   masked_m        NULL (flat) or device int32[E]: live rows of expert e are
  *                   [0, masked_m[e]) (values outside [0, tokens_pad] are clamped).  In
- *                   masked mode nothing outside the live rows is read or written: padding
- *                   rows keep the caller's contents (sglang PR #35593, "Key source
- *                   snippets", test_masked_rows_and_k_tail).
+ *                   masked mode nothing outside the live rows is written or loaded:
+ *                   padding rows keep the caller's contents (sglang PR #35593, "Key source
+ *                   snippets", test_masked_rows_and_k_tail).  A call with expected_m may
+ *                   prefetch its guessed rows (below min(expected_m, tokens_pad)) into L2.
  *   eps             floor of amax; finite and >= PTGQ_EPS_MIN.
  *   stream          CUDA stream of the launch.
  * Returns PTGQ_OK or a negative status.
@@ -214,7 +215,8 @@ int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens, int64_t h
  *   out[e, r, c] = e4m3_satfinite((decode(x[e, r, c]) * x_scale[e, r, c / group_size])
  *                                 * (1 / *output_scale))
  * with binary32 products in that order and a saturating round-to-nearest-even conversion.
- * Rows at or past masked_m[e] are neither read nor written.
+ * Rows at or past masked_m[e] are not written and do not affect the result; the kernel may
+ * read or prefetch some of them (every e < num_experts, r < m lies inside x and x_scale).
  *
  *   x             device e4m3 codes [num_experts, m, k], row-major, 16-byte aligned.
  *   x_scale       device float per-token-group scales; element (e, r, g) at

@@ -178,8 +178,10 @@ def test_requant_speculative_prefetch_stays_inside_x_and_x_scale():
     """ptgq_next.cu, requant_kernel: before the dependency wait each lane prefetches its
     chunk of the warp's first task as if every row were live (c0 = warp * 32 + lane, with
     the slot and row from the same 32-bit divisions as the loop), and that chunk's group
-    scale.  Over shapes, group sizes, chunk widths and grids: whenever r0 < m, the code
-    chunk lies inside x = [E, m, k] and the scale index inside the [E, m, k/G] grid."""
+    scale; after the wait it loads the same chunk and its scale(s) before masked_m is
+    known.  Over shapes, group sizes, chunk widths and grids: whenever r0 < m, the code
+    chunk lies inside x = [E, m, k] and the scale indices (g0, and g0 + 1 when a 32-code
+    chunk spans two groups of 16) inside the [E, m, k/G] grid."""
     for E, m, k, G, V, grid_ctas in itertools.product(
             [1, 3, 8, 33], [1, 5, 64, 1024], [16, 48, 128, 3584], [16, 32, 64, 128], [16, 32],
             [1, 7, 456]):
@@ -198,6 +200,8 @@ def test_requant_speculative_prefetch_stays_inside_x_and_x_scale():
         assert np.all(e0[ok] < E) and np.all(off[ok] >= 0) and np.all(off[ok] + V <= E * m * k)
         g0 = (col0 * V) >> int(np.log2(G))
         assert np.all(g0[ok] < k // G)
+        if V == 32 and G == 16:
+            assert np.all(g0[ok] + 1 < k // G)
 
 
 def test_flat_first_batch_prefetch_stays_inside_x():
