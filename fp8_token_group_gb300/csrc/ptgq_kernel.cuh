@@ -70,10 +70,10 @@ struct Slot {
 // Tuning, per instance (compile-time), from sweeps on GB300: tasks per warp batch, whether
 // the next batch's loads are issued before the current batch is computed, and the CTAs per
 // SM the register budget is sized for.  Without silu: two tasks loaded then computed, 4
-// CTAs/SM (64 registers).  bf16 silu: flat one task pipelined at 3 CTAs/SM; masked two
-// tasks loaded then computed, one CTA of 24 warps per SM (80 registers).  fp16 silu: one
-// CTA of quant_threads() per SM (its table fills most of the shared memory), one task
-// pipelined.
+// CTAs/SM (64 registers).  bf16 silu: one task pipelined, flat at 3 CTAs/SM, masked in one
+// CTA of 24 warps per SM (80 registers; masked silu [32, 384, 2x4096]: 23.09 us against
+// 23.84 us for two tasks loaded then computed).  fp16 silu: one CTA of quant_threads() per
+// SM (its table fills most of the shared memory), one task pipelined.
 // The light flavour of the plain flat instances (kLight): one task per batch at 6 CTAs/SM
 // (40 registers, 48 warps per SM).  It ramps up faster when each warp has only a few
 // tasks, and the launcher takes it below about 8 tasks per warp of the standard grid
@@ -90,8 +90,8 @@ struct Tuning {
   // against 15.2 us round-robin for fp16 silu [8192, 2x2048]; masked silu [32, 384,
   // 2x4096]: 22.9 us round-robin against 23.3 us.)
   static constexpr bool round_robin = f16_silu || (kSilu && kMasked);
-  static constexpr int batch = (f16_silu || kLight || (kSilu && !kMasked)) ? 1 : 2;
-  static constexpr bool pipeline = f16_silu || (kSilu && !kMasked);
+  static constexpr int batch = (kSilu || kLight) ? 1 : 2;
+  static constexpr bool pipeline = kSilu;
   static constexpr int min_blocks = (f16_silu || (kSilu && kMasked)) ? 1 : (kLight ? 6 : (!kSilu ? 4 : 3));
 };
 
@@ -548,11 +548,13 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
       Slot cur;
       Raw16 ca, cb;
       const bool has = first < total_tasks;   // uniform over the warp
-      if (has) issue(yes, first, cur, ca, cb);
+      // The table is waited for before the loads here, unlike in the pipelined loop (hinted
+      // decode batch, bf16 silu: 2.08 us against 2.22 us with the wait after the loads).
       if constexpr (kSilu && Tune::pipeline) {    // uniform: every thread reaches this barrier
         copy_to_smem_wait();
         __syncthreads();
       }
+      if (has) issue(yes, first, cur, ca, cb);
       if (has) finish(cur, ca, cb);
       done = true;
     }
