@@ -234,9 +234,11 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
       build_buckets<kT>(prefix, static_cast<int>(p.n), live_rows, bshift, bucket);
     }
   }
-  // A pipelined instance waits for its table only once its first loads are in flight.
+  // A pipelined instance waits for its table only once its first loads are in flight, or,
+  // in decode-sized masked calls (wlookup), right before its one task (below), so no barrier
+  // is needed here then (unhinted decode batch, bf16 silu: 2.80 -> 2.66 us).
   if constexpr (kSilu && !Tune::pipeline) copy_to_smem_wait();
-  if (kSilu || !wlookup) __syncthreads();
+  if ((kSilu && !Tune::pipeline) || !wlookup) __syncthreads();
   const uint32_t total_units = masked ? live_rows * p.upr : p.units_flat;
 
   const uint32_t lane = threadIdx.x & 31u;
