@@ -72,7 +72,7 @@ def lib() -> ctypes.CDLL:
             L.ptgq_quant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i32, vp, i32, i32, i32, vp,
                                      f32, vp]
             L.ptgq_quant.restype = i32
-            L.ptgq_quant_ex.argtypes = L.ptgq_quant.argtypes + [ctypes.c_uint, i64]
+            L.ptgq_quant_ex.argtypes = L.ptgq_quant.argtypes + [ctypes.c_uint, i64, vp]
             L.ptgq_quant_ex.restype = i32
             L.ptgq_scale_elems.argtypes = [i64, i64, i64, i32, i32, i32, i32,
                                            ctypes.POINTER(i64)]
@@ -147,11 +147,12 @@ def alloc_outputs(x, group_size: int, *, out_dtype: int = E4M3, scale_fmt: int =
 def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
           scale_fmt: int = SCALE_FP32, scale_layout: int = ROW_MAJOR, fuse_silu: bool = False,
           masked_m=None, eps: float = 1e-10, tokens_pad: int = 0, flags: int = 0,
-          expected_m: int = 0, stream=None) -> None:
+          expected_m: int = 0, masked_m_errors=None, stream=None) -> None:
     """Quantize ``x`` into the caller's ``out_q`` / ``out_s`` on ``stream`` (default: torch's
     current stream).  Tensors must be device-accessible: CUDA tensors, or pinned host tensors,
     which the GPU reads and writes in place over the host link (unified addressing).
-    Arguments follow ``ptgq_quant`` in include/ptgq.h."""
+    Arguments follow ``ptgq_quant_ex`` in include/ptgq.h; ``masked_m_errors`` is an optional
+    device int32 tensor that counts masked_m entries outside [0, tokens_pad]."""
     import torch
     all_cuda = x.is_cuda and out_q.is_cuda and out_s.is_cuda
     if not all_cuda:
@@ -191,12 +192,17 @@ def quant(x, out_q, out_s, group_size: int, *, out_dtype: int | None = None,
                              f"the call writes up to {need_s}")
     if masked_m is not None and masked_m.numel() < n:
         raise ValueError(f"masked_m has {masked_m.numel()} entries for {n} experts")
+    err_ptr = None
+    if masked_m_errors is not None:
+        if masked_m_errors.dtype != torch.int32 or not masked_m_errors.is_cuda:
+            raise ValueError("masked_m_errors must be an int32 CUDA tensor")
+        err_ptr = masked_m_errors.data_ptr()
     handle = _stream_handle(stream, x.get_device() if x.is_cuda else None)
     rc = (_lib or lib()).ptgq_quant_ex(
         x.data_ptr(), _in_dtype(x), n, tokens_pad, H, group_size, out_q.data_ptr(), out_dtype,
         out_s.data_ptr(), scale_fmt, scale_layout, int(bool(fuse_silu)),
         None if masked_m is None else masked_m.data_ptr(), float(eps), handle, flags,
-        int(expected_m))
+        int(expected_m), err_ptr)
     if rc != 0:
         raise PtgqError(rc)
 

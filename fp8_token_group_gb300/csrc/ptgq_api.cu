@@ -178,18 +178,60 @@ int launch_blocks(const void* fn, int dev, size_t smem, int threads, int* blocks
 
 using namespace ptgq;
 
+namespace ptgq {
+namespace masked_count {
+
+// The optional out-of-range count of ptgq_quant_ex: one CTA adds the number of experts whose
+// masked_m lies outside [0, rows] to *err.  A kernel of its own, launched after the quantizer
+// in stream order only when the caller asks for the count, so the quantizer's code is the
+// same whether or not it is counted (counting inside its masked prologue cost the fp16
+// masked silu call 2%).
+__global__ void __launch_bounds__(256) masked_m_error_kernel(const int32_t* __restrict__ masked_m,
+                                                             int64_t n, int64_t rows,
+                                                             int32_t* err) {
+  int bad = 0;
+  for (int64_t e = threadIdx.x; e < n; e += blockDim.x) {
+    const int32_t m = masked_m[e];
+    bad += (m < 0 || m > rows) ? 1 : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xFFFFFFFFu, bad, o);
+  if ((threadIdx.x & 31u) == 0u && bad != 0) atomicAdd(err, bad);
+}
+
+int count_masked_errors(const int32_t* masked_m, int64_t n, int64_t rows, int32_t* err,
+                        ptgq_stream_t stream) {
+  if (err == nullptr || masked_m == nullptr || n == 0) return PTGQ_OK;
+  void* args[] = {&masked_m, &n, &rows, &err};
+  // As for the quantizer's launch: only this launch's own failure is reported and cleared.
+  if (cudaLaunchKernel(reinterpret_cast<const void*>(&masked_m_error_kernel), dim3(1), dim3(256),
+                       args, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return PTGQ_ERR_CUDA;
+  }
+  return PTGQ_OK;
+}
+
+}  // namespace masked_count
+}  // namespace ptgq
+
 extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens_pad,
                              int64_t hidden, int group_size, void* out_q, int out_dtype,
                              void* out_s, int scale_fmt, int scale_layout, int fuse_silu,
                              const int32_t* masked_m, float eps, ptgq_stream_t stream,
-                             unsigned flags, int64_t expected_m) {
+                             unsigned flags, int64_t expected_m, int32_t* masked_m_errors) {
   Geometry g;
   int rc = validate(x, dtype, n, tokens_pad, hidden, group_size, out_q, out_dtype, out_s,
                     scale_fmt, scale_layout, fuse_silu, masked_m, eps, flags, &g);
   if (rc != PTGQ_OK) return rc;
   if (expected_m < 0) return PTGQ_ERR_SHAPE;
   const bool masked = masked_m != nullptr;
-  if (g.blocks * g.rows == 0) return PTGQ_OK;   // nothing to read or write
+  if (masked && masked_m_errors != nullptr &&
+      reinterpret_cast<uintptr_t>(masked_m_errors) % 4 != 0)
+    return PTGQ_ERR_ALIGN;
+  using ptgq::masked_count::count_masked_errors;
+  if (g.blocks * g.rows == 0)                   // nothing to read or write
+    return masked ? count_masked_errors(masked_m, n, g.rows, masked_m_errors, stream) : PTGQ_OK;
 
   Params p{};
   p.x = x;
@@ -298,7 +340,7 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
     cudaGetLastError();
     return PTGQ_ERR_CUDA;
   }
-  return PTGQ_OK;
+  return masked ? count_masked_errors(masked_m, n, g.rows, masked_m_errors, stream) : PTGQ_OK;
 }
 
 extern "C" int ptgq_quant(const void* x, int dtype, int64_t n, int64_t tokens_pad, int64_t hidden,
@@ -306,7 +348,7 @@ extern "C" int ptgq_quant(const void* x, int dtype, int64_t n, int64_t tokens_pa
                           int scale_layout, int fuse_silu, const int32_t* masked_m, float eps,
                           ptgq_stream_t stream) {
   return ptgq_quant_ex(x, dtype, n, tokens_pad, hidden, group_size, out_q, out_dtype, out_s,
-                       scale_fmt, scale_layout, fuse_silu, masked_m, eps, stream, 0u, 0);
+                       scale_fmt, scale_layout, fuse_silu, masked_m, eps, stream, 0u, 0, nullptr);
 }
 
 extern "C" int ptgq_scale_elems(int64_t n, int64_t tokens_pad, int64_t hidden, int group_size,

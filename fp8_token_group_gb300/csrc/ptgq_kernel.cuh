@@ -265,7 +265,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
   // WS (masked calls with wlookup): the expert comes from the warp's w_key, else from the
   // shared-memory prefix and buckets.
   auto issue = [&](auto ws, uint32_t t, Slot& sl, Raw16& a, Raw16& b) {
-    constexpr bool WS = decltype(ws)::value;
+    [[maybe_unused]] constexpr bool WS = decltype(ws)::value;
     const uint32_t u0 = (t << upw_log2) + lane_unit;
     sl.unit_valid = u0 < total_units;
     const uint32_t u = sl.unit_valid ? u0 : total_units - 1u;

@@ -156,8 +156,8 @@ enum {
   PTGQ_FLAG_FAST_DIVIDE = 4
 };
 
-/* ptgq_quant with option flags (a bitwise OR of PTGQ_FLAG_*) and a hint;
- * flags == 0 and expected_m == 0 is ptgq_quant.
+/* ptgq_quant with option flags (a bitwise OR of PTGQ_FLAG_*), a hint and an error counter;
+ * flags == 0, expected_m == 0 and masked_m_errors == NULL is ptgq_quant.
  *   expected_m  masked mode: the caller's estimate of the live rows per expert (sglang PR
  *               #30924, "Implementation breakdown" item 2: the custom op takes masked_m
  *               and expected_m).  The live counts sit in device memory, so without a hint
@@ -169,11 +169,18 @@ enum {
  *               live counts are known (a cache hint: their contents never reach the
  *               outputs), so x must span its whole [E, tokens_pad, H_in] extent, as
  *               ptgq_quant requires.  0: no hint.  Ignored in flat mode.
- *               Negative: PTGQ_ERR_SHAPE. */
+ *               Negative: PTGQ_ERR_SHAPE.
+ *   masked_m_errors  masked mode: NULL, or a 4-byte aligned device int32 to which the call
+ *               adds the number of experts e < E whose masked_m[e] lies outside
+ *               [0, tokens_pad] (such counts are clamped, never a fault).  A second kernel
+ *               of one CTA, launched after the quantizer on the same stream, adds it with
+ *               atomic adds, so calls on several streams may share the counter.  The caller
+ *               zeroes it and reads it after the stream's work.  Ignored in flat mode. */
 int ptgq_quant_ex(const void* x, int dtype, int64_t num_tokens_or_E, int64_t tokens_pad,
                   int64_t hidden, int group_size, void* out_q, int out_dtype, void* out_s,
                   int scale_fmt, int scale_layout, int fuse_silu, const int32_t* masked_m,
-                  float eps, ptgq_stream_t stream, unsigned flags, int64_t expected_m);
+                  float eps, ptgq_stream_t stream, unsigned flags, int64_t expected_m,
+                  int32_t* masked_m_errors);
 
 /* Size helper: the number of scale elements (floats, or int32 words for the packed format)
  * that out_s must hold for these arguments (masked != 0 selects the masked layout, where

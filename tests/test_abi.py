@@ -71,11 +71,12 @@ def test_scale_elems_matches_oracle(L, fmt, layout, masked):
 
 def _call(L, **kw):
     a = dict(x=32, dtype=0, n=4, tokens_pad=0, hidden=256, group=128, q=16, out=0, s=4, fmt=0,
-             layout=0, silu=0, mm=None, eps=1e-10, stream=None, flags=0, expected_m=0)
+             layout=0, silu=0, mm=None, eps=1e-10, stream=None, flags=0, expected_m=0,
+             errors=None)
     a.update(kw)
     return L.ptgq_quant_ex(a["x"], a["dtype"], a["n"], a["tokens_pad"], a["hidden"], a["group"],
                            a["q"], a["out"], a["s"], a["fmt"], a["layout"], a["silu"], a["mm"],
-                           a["eps"], a["stream"], a["flags"], a["expected_m"])
+                           a["eps"], a["stream"], a["flags"], a["expected_m"], a["errors"])
 
 
 def test_validation_codes(L):
@@ -98,6 +99,7 @@ def test_validation_codes(L):
     assert _call(L, silu=2) == -11
     assert _call(L, flags=8) == -11
     assert _call(L, mm=64, tokens_pad=8, expected_m=-1) == -6
+    assert _call(L, mm=64, n=4, tokens_pad=8, errors=2) == -7   # masked_m_errors 4-byte aligned
     assert _call(L, x=0) == -1
     assert _call(L, q=0) == -1
     assert _call(L, s=0) == -1

@@ -447,6 +447,35 @@ def test_masked_expert_lookup_around_32_experts(E, dt, silu, size):
             compare(x, c, masked_m=mm)
 
 
+@pytest.mark.parametrize("E", [6, 32, 33, 1000])
+@pytest.mark.parametrize("silu", [False, True])
+def test_masked_m_error_counter(E, silu):
+    """The optional masked_m_errors counter of ptgq_quant_ex: each call adds the number of
+    experts whose masked_m lies outside [0, tokens_pad], for the warp-scanned (E <= 32) and
+    the block-wide (E > 32) prefix, decode-sized and larger calls; the outputs stay those of
+    the clamped counts (oracle), and a second call adds again."""
+    rng = np.random.default_rng(E + 7 * silu)
+    tp, H = 23, 256
+    mm = rng.integers(0, tp + 1, E)
+    bad = rng.random(E) < 0.25
+    mm[bad] = np.where(rng.random(int(bad.sum())) < 0.5, -rng.integers(1, 5, int(bad.sum())),
+                       tp + rng.integers(1, 40, int(bad.sum())))
+    mm[0] = -1
+    mm = mm.astype(np.int32)
+    want = int(((mm < 0) | (mm > tp)).sum())
+    x = synth.sweep_input(E + 3, E * tp, 2 * H if silu else H, torch.bfloat16).reshape(E, tp, -1)
+    xd = x.cuda()
+    md = torch.from_numpy(mm).cuda()
+    errs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for hint in (0, 1):
+        q, sc = P.alloc_outputs(xd, 128, scale_fmt=P.SCALE_UE8M0_PACKED, fuse_silu=silu, masked=True)
+        P.quant(xd, q, sc, 128, scale_fmt=P.SCALE_UE8M0_PACKED, fuse_silu=silu, masked_m=md,
+                expected_m=hint, masked_m_errors=errs)
+    torch.cuda.synchronize()
+    assert int(errs.item()) == 2 * want
+    compare(x, Case(silu=silu, scale_fmt=P.SCALE_UE8M0_PACKED), masked_m=mm)
+
+
 def test_many_experts():
     E = 1000
     x = synth.normal((E, 4, 256), torch.bfloat16, seed=2)
