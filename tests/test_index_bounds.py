@@ -206,13 +206,19 @@ def test_requant_speculative_prefetch_stays_inside_x_and_x_scale():
 
 def test_flat_first_batch_prefetch_stays_inside_x():
     """ptgq_kernel.cuh: before the dependency wait every flat warp prefetches its first
-    batch (the first task and, with two-task batches, the task a grid stride further): units
+    batch (the first task and, with two-task batches or in a light call of at most three
+    tasks per warp, the task a grid stride further): units
     below the call's units, groups below the row's groups.  Over shapes, group sizes, scale
     formats, silu, batch sizes, both dealings and grids larger and smaller than the work,
     every prefetched chunk (gate and, with silu, up) lies inside x = [T, H_in]."""
     for T, H, G, packed, silu, kB, rr, grid in itertools.product(
-            [1, 7, 64, 333], [128, 384, 2048], [16, 32, 64, 128], [0, 1], [0, 1], [1, 2],
+            [1, 7, 64, 333], [128, 384, 2048], [16, 32, 64, 128], [0, 1], [0, 1], [1, 2, "light"],
             [0, 1], [1, 6, 600]):
+        light = kB == "light"
+        if light:
+            kB = 1
+            if silu or rr:
+                continue                  # the light flavour is plain flat, tasks in blocks
         if H % G:
             continue
         lg_log2 = {16: 0, 32: 1, 64: 2, 128: 3}[G]
@@ -231,6 +237,8 @@ def test_flat_first_batch_prefetch_stays_inside_x():
         use_rr = rr and tasks < stride
         t0 = b + grid * w if use_rr else b * warps + w
         nb = 1 if (kB > 1 and tasks <= stride) else kB
+        if light and tasks <= 3 * stride:
+            nb = 2                        # the light flavour's second task, for <= 3 per warp
         local = lane & ((1 << lu) - 1)
         for bb in range(nb):
             u = ((t0 + bb * stride) << upw_log2) + (lane >> lu)
