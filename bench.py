@@ -382,6 +382,14 @@ class RequantWorkload(Workload):
         P.requant_per_tensor(xd, xs, mm, self._scale, out, group_size=128)
 
 
+def _sweep_index(T: int, H: int, dt: str) -> int:
+    """The sweep case index whose seeded input the [T, H] shape of dtype dt uses (its G = 16,
+    e4m3 case, as in large_sweep)."""
+    from fp8_token_group_gb300 import synth
+    return {(c[1], c[2], str(c[3])[6:], c[4], c[5]): c[0]
+            for c in synth.sweep_cases()}[(T, H, dt, 16, "e4m3")]
+
+
 def workloads():
     from fp8_token_group_gb300 import synth
     import torch
@@ -414,6 +422,10 @@ def workloads():
         "sweep_big": Workload("sweep_big", "flat bf16 [32768,7168] N(0,1), G=128, e4m3, fp32 "
                               "row-major", lambda: synth.normal((32768, 7168), torch.bfloat16,
                                                                 seed=1)),
+        "flat_mid": Workload("flat_mid", "flat bf16 [4096,2048] (the shape sweep's input recipe), "
+                             "G=128, e4m3, fp32 row-major: the sweep's smallest large shape",
+                             lambda: synth.sweep_input(_sweep_index(4096, 2048, "bfloat16"), 4096,
+                                                       2048, torch.bfloat16)),
         "per_token": PerTokenWorkload("per_token", "per-token FP8 quant, bf16 [4096,4096] "
                                       "N(0,1) -> e4m3 + fp32 scale per row", 4096, 4096),
         "requant": RequantWorkload("requant", "per-token-group -> per-tensor FP8 requant, e4m3 "
@@ -921,7 +933,8 @@ def main():
     ap.add_argument("--workload", default="flat_outliers",
                     choices=["flat_outliers", "flat_small", "silu_flat", "masked_silu",
                              "silu_flat_fp16", "masked_silu_fp16", "masked_decode",
-                             "masked_decode_hint", "sweep_big", "per_token", "requant"], help="workload of the JSON line (default: the "
+                             "masked_decode_hint", "sweep_big", "flat_mid", "per_token", "requant"],
+                    help="workload of the JSON line (default: the "
                     "benchmarked flat_outliers)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
