@@ -292,7 +292,11 @@ extern "C" int ptgq_quant_ex(const void* x, int dtype, int64_t n, int64_t tokens
     fn = kernel_for(key);
     rc = launch_blocks(fn, dev, smem, threads, &per_sm, &sms);
     if (rc != PTGQ_OK) return rc;
-    if (tasks > static_cast<int64_t>(per_sm) * sms * kWarps) {
+    // Above three tasks per warp of the light grid, the instances with the next-batch
+    // prefetch; up to three, the kernel prefetches a warp's first two tasks before its
+    // dependency wait instead, and the rolling prefetch only costs issue slots ([4096, 2048]:
+    // 5.23 -> 4.92 us, [1024, 7168]: 4.55 -> 4.24 us without it).
+    if (tasks > 3 * static_cast<int64_t>(per_sm) * sms * kWarps) {
       key.light = 2;
       p.prefetch_next = 1u;
       fn = kernel_for(key);
