@@ -42,8 +42,9 @@ def _per_token_both(x: torch.Tensor, out_rows: int):
 def test_per_token_vs_oracle(dt, hidden, T):
     """Token counts below and at 16 x SMs (the pages' warp/CTA dispatch threshold) and the
     benchmarked 4096, row lengths that are multiples of 4 but not 8, zero rows, integer
-    rows, padded output.  The launch shapes cover one buffer per warp (one round of rows)
-    and two (several rounds)."""
+    rows, padded output.  The launch shapes cover one CTA per row (T <= 4 x SMs, rows of 16-byte
+    multiples, including rows longer than the CTA keeps in registers), one buffer per warp
+    (one round of rows) and two (several rounds)."""
     x = synth.sweep_input(hidden + T, T, hidden, torch.float32)
     x[::7] = 0
     x = x.to(dt)
@@ -122,8 +123,8 @@ def test_per_token_row_sizes_in_any_order():
 def test_per_token_reciprocal_overflow_fixture_and_tiny_rows():
     """Rows whose reciprocal scale overflows (max below about 1.3e-36) take the page's clamp
     (0 * inf = NaN clamps to +448); the hand-worked fixture rows, then random tiny rows of
-    every dtype through the staged kernel (hidden 512) and the register kernel (hidden 4,
-    1076), mixed with ordinary rows in the same call."""
+    every dtype through the CTA-per-row kernel (hidden 512) and the register kernel (hidden
+    4, 1076), mixed with ordinary rows in the same call."""
     from golden_fixtures import per_token_overflow_rows
     for dt, bits, want in per_token_overflow_rows():
         if dt == "fp32":
