@@ -137,11 +137,13 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
   //   flat  : the exact tasks of the first batch (the first task and the batch's strides).
   //   masked: with a hint of the live rows per expert, the rows of the first task guessed
   //           as if every expert had exactly rows_hint live rows (hinted decode batch, bf16
-  //           silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us).  The guess only decides
-  //           what is prefetched: rows below rows_hint <= rows of experts below n, so every
-  //           prefetched address lies inside x.  Calls without a hint prefetch nothing: a
-  //           guess of one row per expert gained 0.08 us on the unhinted decode batch but
-  //           cost 0.15-0.18 us on the large masked silu calls.
+  //           silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us); without one, as if every
+  //           expert had one live row, the rows a decode batch has (unhinted decode batch,
+  //           bf16 silu: 2.78 -> 2.00 us, plain 2.33 -> 2.07 us, large masked silu 23.05 ->
+  //           22.90 us; not in the fp16 silu instances, whose large masked call it made 17%
+  //           slower).  The guess only decides what is prefetched: rows below
+  //           max(rows_hint, 1) <= rows of experts below n, so every prefetched address lies
+  //           inside x.
   {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t lu_log2 = p.lg_log2 + p.ug_log2;
@@ -154,13 +156,15 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
       if constexpr (kSilu) prefetch_l2(src + p.hidden);
     };
     if constexpr (kMasked) {
-      if (p.rows_hint > 0u) {
+      if (p.rows_hint > 0u || !Tune::f16_silu) {
+        const uint32_t rh = p.rows_hint > 0u ? p.rows_hint : 1u;
+        const uint32_t rhm = p.rows_hint > 0u ? p.rows_hint_magic : 0xFFFFFFFFu;
         const uint32_t u = (first_task(Tune::round_robin) << (5u - lu_log2)) + (lane >> lu_log2);
         const uint32_t R = udiv(u, p.upr, p.upr_magic);
-        const uint32_t e = udiv(R, p.rows_hint, p.rows_hint_magic);
+        const uint32_t e = udiv(R, rh, rhm);
         const uint32_t g = ((u - R * p.upr) << p.ug_log2) + (local >> p.lg_log2);
         if (e < p.n && g < p.ng)
-          prefetch_row(static_cast<int64_t>(e) * p.rows + (R - e * p.rows_hint), g);
+          prefetch_row(static_cast<int64_t>(e) * p.rows + (R - e * rh), g);
       }
     } else {
       const uint32_t upw_log2 = 5u - lu_log2;

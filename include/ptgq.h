@@ -121,8 +121,9 @@ enum {
  *                   [0, masked_m[e]) (values outside [0, tokens_pad] are clamped).  In
  *                   masked mode nothing outside the live rows is written or loaded:
  *                   padding rows keep the caller's contents (sglang PR #35593, "Key source
- *                   snippets", test_masked_rows_and_k_tail).  A call with expected_m may
- *                   prefetch its guessed rows (below min(expected_m, tokens_pad)) into L2.
+ *                   snippets", test_masked_rows_and_k_tail).  A call may prefetch guessed
+ *                   rows into L2 (row 0 of each expert, or with expected_m the rows below
+ *                   min(expected_m, tokens_pad)); their contents never reach the outputs.
  *   eps             floor of amax; finite and >= PTGQ_EPS_MIN.
  *   stream          CUDA stream of the launch.
  * Returns PTGQ_OK or a negative status.
@@ -164,10 +165,10 @@ enum {
  *               the grid is sized for every row of tokens_pad being live; with one it is
  *               sized for E * min(expected_m, tokens_pad) rows.  Results are the same for
  *               any value: the grid strides over whatever rows are live, so a low hint
- *               costs time, never correctness.  With a hint, rows below
- *               min(expected_m, tokens_pad) of x may be prefetched into L2 before the
- *               live counts are known (a cache hint: their contents never reach the
- *               outputs), so x must span its whole [E, tokens_pad, H_in] extent, as
+ *               costs time, never correctness.  Rows below min(expected_m, tokens_pad)
+ *               of x (row 0 of each expert without a hint) may be prefetched into L2
+ *               before the live counts are known (a cache hint: their contents never reach
+ *               the outputs), so x must span its whole [E, tokens_pad, H_in] extent, as
  *               ptgq_quant requires.  0: no hint.  Ignored in flat mode.
  *               Negative: PTGQ_ERR_SHAPE.
  *   masked_m_errors  masked mode: NULL, or a 4-byte aligned device int32 to which the call

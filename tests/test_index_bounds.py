@@ -85,16 +85,17 @@ def _udiv(n, d, magic):
 
 
 def test_hint_prefetch_stays_inside_x():
-    """With an expected_m hint every masked CTA guesses the rows of its warps' first tasks
-    (each expert taken to have min(expected_m, tokens_pad) live rows) and prefetches them.
-    Over shapes, group sizes, scale formats, silu, hints, both task dealings and more warps
-    than tasks, every prefetched 32-byte chunk (gate and, with silu, up) lies inside
-    x = [E, tokens_pad, H_in]."""
+    """Every masked CTA guesses the rows of its warps' first tasks (each expert taken to have
+    min(expected_m, tokens_pad) live rows with a hint, one without: hint 0 below) and
+    prefetches them.  Over shapes, group sizes, scale formats, silu, hints, both task
+    dealings and more warps than tasks, every prefetched 32-byte chunk (gate and, with silu,
+    up) lies inside x = [E, tokens_pad, H_in]."""
     for E, rows, H, G, packed, silu, hint, rr in itertools.product(
             [1, 3, 32], [1, 5, 40], [128, 384, 2048], [16, 32, 64, 128], [0, 1], [0, 1],
-            [1, 3, 7, 1000], [0, 24, 32]):
+            [0, 1, 3, 7, 1000], [0, 24, 32]):
         if H % G:
             continue
+        hint = hint or 1                  # no hint: one live row per expert
         lg_log2 = {16: 0, 32: 1, 64: 2, 128: 3}[G]
         ug_log2 = 2 if packed else 0
         ng = H // G
