@@ -196,24 +196,26 @@ __global__ void __launch_bounds__(kThreads) per_token_smem_kernel(const PerToken
 // One CTA per row, for calls with few rows (the pages' per-token CTA variant, sglang PR
 // #34257, "Key source snippets": chosen below 16 x SMs rows).  With one warp per row, a call
 // of a few hundred rows leaves most of the GPU idle and each warp moves its whole row by
-// itself; here the CTA's 8 warps split the row, the row max is combined through shared
+// itself; here the CTA's kT / 32 warps (8, or 4 for calls of a little more rows) split the
+// row, the row max is combined through shared
 // memory, and the first kCache 16-byte chunks of each thread stay in registers between the
 // max pass and the quantize pass (the rest are read again, from L2).  Rows must be a
 // multiple of 16 bytes and 16-byte aligned.  The CTA's first row goes to L2 before the
 // dependency wait.  The arithmetic is that of the other per-token kernels.
-template <int kIn>
-__global__ void __launch_bounds__(kThreads) per_token_cta_kernel(const PerTokenParams p) {
+template <int kIn, int kT>
+__global__ void __launch_bounds__(kT) per_token_cta_kernel(const PerTokenParams p) {
   constexpr int kEsize = kIn == 2 ? 4 : 2;
   constexpr int kPer16 = 16 / kEsize;
   constexpr int kCache = 4;
-  __shared__ uint32_t wmax[2][kWarps];
+  constexpr int kW = kT / 32;
+  __shared__ uint32_t wmax[2][kW];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t chunks = p.hidden / kPer16;
   const int64_t row_bytes = chunks * 16;
   const char* xb = static_cast<const char*>(p.x);
   if (blockIdx.x < p.tokens) {
     const char* r = xb + static_cast<int64_t>(blockIdx.x) * row_bytes;
-    for (int64_t o = static_cast<int64_t>(tid) * 128; o < row_bytes; o += kThreads * 128)
+    for (int64_t o = static_cast<int64_t>(tid) * 128; o < row_bytes; o += kT * 128)
       prefetch_l2(r + o);
   }
   griddep_wait();
@@ -229,13 +231,13 @@ __global__ void __launch_bounds__(kThreads) per_token_cta_kernel(const PerTokenP
     uint32_t m = 0u;
 #pragma unroll
     for (int j = 0; j < kCache; ++j) {
-      const int64_t c = tid + static_cast<int64_t>(j) * kThreads;
+      const int64_t c = tid + static_cast<int64_t>(j) * kT;
       if (c < chunks) {
         load(src, c, cache[j]);
         m = absmax_words<kIn>(m, cache[j], 4);
       }
     }
-    for (int64_t c = tid + static_cast<int64_t>(kCache) * kThreads; c < chunks; c += kThreads) {
+    for (int64_t c = tid + static_cast<int64_t>(kCache) * kT; c < chunks; c += kT) {
       uint32_t w[4];
       load(src, c, w);
       m = absmax_words<kIn>(m, w, 4);
@@ -247,20 +249,20 @@ __global__ void __launch_bounds__(kThreads) per_token_cta_kernel(const PerTokenP
     __syncthreads();
     uint32_t mm = 0u;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mm = max(mm, wmax[par][w]);
+    for (int w = 0; w < kW; ++w) mm = max(mm, wmax[par][w]);
     const float s = __fdiv_rn(u2f(mm), 448.0f);
     const float inv = s == 0.0f ? 0.0f : __frcp_rn(s);
     const bool clamp = row_needs_clamp(s, inv);
     uint8_t* qrow = p.q + row * p.hidden;
 #pragma unroll
     for (int j = 0; j < kCache; ++j) {
-      const int64_t c = tid + static_cast<int64_t>(j) * kThreads;
+      const int64_t c = tid + static_cast<int64_t>(j) * kT;
       if (c < chunks) {
         if (clamp) quantize16_clamped<kIn>(cache[j], inv, qrow + c * kPer16);
         else quantize16<kIn>(cache[j], inv, qrow + c * kPer16);
       }
     }
-    for (int64_t c = tid + static_cast<int64_t>(kCache) * kThreads; c < chunks; c += kThreads) {
+    for (int64_t c = tid + static_cast<int64_t>(kCache) * kT; c < chunks; c += kT) {
       uint32_t w[4];
       load(src, c, w);
       if (clamp) quantize16_clamped<kIn>(w, inv, qrow + c * kPer16);
@@ -660,16 +662,25 @@ const void* per_token_reg_fn(int dtype, bool wide) {
   }
 }
 
-const void* per_token_cta_fn(int dtype) {
-  switch (dtype) {
-    case 0: return reinterpret_cast<const void*>(&per_token_cta_kernel<0>);
-    case 1: return reinterpret_cast<const void*>(&per_token_cta_kernel<1>);
-    default: return reinterpret_cast<const void*>(&per_token_cta_kernel<2>);
+const void* per_token_cta_fn(int dtype, int threads) {
+  switch (dtype * 2 + (threads == 128 ? 1 : 0)) {
+    case 0: return reinterpret_cast<const void*>(&per_token_cta_kernel<0, 256>);
+    case 1: return reinterpret_cast<const void*>(&per_token_cta_kernel<0, 128>);
+    case 2: return reinterpret_cast<const void*>(&per_token_cta_kernel<1, 256>);
+    case 3: return reinterpret_cast<const void*>(&per_token_cta_kernel<1, 128>);
+    case 4: return reinterpret_cast<const void*>(&per_token_cta_kernel<2, 256>);
+    default: return reinterpret_cast<const void*>(&per_token_cta_kernel<2, 128>);
   }
 }
 
 // Calls of at most this many rows per SM take the CTA-per-row kernel.
 constexpr int64_t kPtCtaRowsPerSm = 4;
+// Calls of at most this many rows per SM (and more than kPtCtaRowsPerSm), with rows of at
+// most kPtHalfCtaRowBytes, take CTAs of 4 warps per row ([1024, 4096]: 3.09 -> 2.81 us,
+// [1600, 4096]: 4.05 -> 3.72 us, [1216, 7168]: 5.19 -> 5.04 us; longer rows re-read more of
+// themselves from L2 with half the threads, [1024, 16384]: 10.08 -> 11.91 us).
+constexpr int64_t kPtHalfCtaRowsPerSm = 12;
+constexpr int64_t kPtHalfCtaRowBytes = 16 * 1024;
 
 const void* per_token_smem_fn(int dtype, int bufs) {
   switch (dtype * 2 + (bufs == 2 ? 1 : 0)) {
@@ -754,12 +765,16 @@ extern "C" int ptgq_per_token_quant(const void* x, int dtype, int64_t num_tokens
   // which two fit in a CTA's shared memory.
   const int64_t row_bytes = hidden * esize;
   if (row_bytes % 16 == 0 && row_bytes >= 512 && reinterpret_cast<uintptr_t>(x) % 16 == 0) {
-    const void* fn = per_token_cta_fn(dtype);
-    int bps = 0, sms = 0;
-    if (occupancy(fn, 0, kThreads, &bps, &sms) != 0) return PTGQ_ERR_CUDA;
-    if (num_tokens <= kPtCtaRowsPerSm * sms) {
-      const int grid = static_cast<int>(std::min<int64_t>(num_tokens, static_cast<int64_t>(bps) * sms));
-      return launch(fn, grid, 0, stream, args);
+    for (const int threads : {256, 128}) {
+      const void* fn = per_token_cta_fn(dtype, threads);
+      int bps = 0, sms = 0;
+      if (occupancy(fn, 0, threads, &bps, &sms) != 0) return PTGQ_ERR_CUDA;
+      const int64_t limit = threads == 256 ? kPtCtaRowsPerSm * sms
+                            : (row_bytes <= kPtHalfCtaRowBytes ? kPtHalfCtaRowsPerSm * sms : 0);
+      if (num_tokens <= limit) {
+        const int grid = static_cast<int>(std::min<int64_t>(num_tokens, static_cast<int64_t>(bps) * sms));
+        return launch(fn, grid, 0, stream, args, threads);
+      }
     }
   }
   if (row_bytes % 16 == 0 && row_bytes >= 512 && 2 * row_bytes <= 227 * 1024 &&

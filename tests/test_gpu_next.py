@@ -38,13 +38,14 @@ def _per_token_both(x: torch.Tensor, out_rows: int):
 
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("hidden", [4, 128, 1076, 1368, 4096, 7168, 16384])
-@pytest.mark.parametrize("T", [1, 39, 2432, 4096])
+@pytest.mark.parametrize("T", [1, 39, 1000, 2432, 4096])
 def test_per_token_vs_oracle(dt, hidden, T):
     """Token counts below and at 16 x SMs (the pages' warp/CTA dispatch threshold) and the
     benchmarked 4096, row lengths that are multiples of 4 but not 8, zero rows, integer
-    rows, padded output.  The launch shapes cover one CTA per row (T <= 4 x SMs, rows of 16-byte
-    multiples, including rows longer than the CTA keeps in registers), one buffer per warp
-    (one round of rows) and two (several rounds)."""
+    rows, padded output.  The launch shapes cover one CTA per row (8 warps for T <= 4 x SMs,
+    4 warps for T <= 12 x SMs with rows up to 16 KB; rows of 16-byte multiples, including rows
+    longer than the CTA keeps in registers), one buffer per warp (one round of rows) and two
+    (several rounds)."""
     x = synth.sweep_input(hidden + T, T, hidden, torch.float32)
     x[::7] = 0
     x = x.to(dt)
