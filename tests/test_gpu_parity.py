@@ -518,6 +518,35 @@ def test_back_to_back_launches_and_cuda_graph():
     assert torch.equal(q3.view(torch.uint8), ref_q.view(torch.uint8)) and torch.equal(s3, ref_s)
 
 
+def test_masked_calls_and_error_counter_in_a_cuda_graph():
+    """A masked call with the masked_m error counter (two kernels per call) captured in a CUDA
+    graph with its masked_m and replayed: the outputs match an eager call, and the counter
+    grows by the out-of-range count on every replay."""
+    x, mm = synth.masked_silu(experts=8, tokens_pad=64, hidden=512)
+    mm = mm.clone()
+    mm[1], mm[5] = -2, 90
+    xd, md = x.cuda(), mm.cuda()
+    q, sc = P.alloc_outputs(xd, 128, fuse_silu=True, masked=True, scale_fmt=P.SCALE_UE8M0_PACKED)
+    q.view(torch.uint8).fill_(0x2C)
+    sc.fill_(0x2C2C2C2C)
+    P.quant(xd, q, sc, 128, fuse_silu=True, masked_m=md, scale_fmt=P.SCALE_UE8M0_PACKED)
+    torch.cuda.synchronize()
+    ref_q, ref_s = q.clone(), sc.clone()
+    q2, s2 = q.clone().fill_(0), sc.clone().fill_(0)
+    q2.view(torch.uint8).fill_(0x2C)
+    s2.fill_(0x2C2C2C2C)
+    errs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        P.quant(xd, q2, s2, 128, fuse_silu=True, masked_m=md, scale_fmt=P.SCALE_UE8M0_PACKED,
+                masked_m_errors=errs)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(q2.view(torch.uint8), ref_q.view(torch.uint8)) and torch.equal(s2, ref_s)
+    assert int(errs.item()) == 3 * 2
+
+
 def test_device_arguments_rejected_before_launch():
     x = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
     q, s = P.alloc_outputs(x, 128)
