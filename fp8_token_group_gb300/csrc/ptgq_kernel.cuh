@@ -122,8 +122,13 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
   };
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + Tab::bytes);
 
-  // Module constants first (asynchronously): they do not depend on the previous grid.
-  if constexpr (kSilu) {
+  // Module constants first (asynchronously): they do not depend on the previous grid.  The
+  // masked fp16 silu instances issue their 162 KB table copy after the row prefetches below
+  // instead (with the copy first, the unhinted guess made the large masked call 17% slower;
+  // after them, the unhinted decode batch 2.75 -> 2.59 us and the large call 22.58 -> 22.49
+  // us), the others before.
+  constexpr bool kCopyFirst = !(kFp16 && kSilu && kMasked);
+  if constexpr (kSilu && kCopyFirst) {
     if constexpr (kFp16) copy_to_smem_async<kT>(smem, kSiluF16, kSiluF16Words / 4);
     else copy_to_smem_async<kT>(smem, kSiluBf16, kSiluBf16Words / 4);
   }
@@ -140,8 +145,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
   //           silu: 3.16 -> 2.91 us; fp16 silu: 3.68 -> 3.62 us); without one, as if every
   //           expert had one live row, the rows a decode batch has (unhinted decode batch,
   //           bf16 silu: 2.78 -> 2.00 us, plain 2.33 -> 2.07 us, large masked silu 23.05 ->
-  //           22.90 us; not in the fp16 silu instances, whose large masked call it made 17%
-  //           slower).  The guess only decides what is prefetched: rows below
+  //           22.90 us).  The guess only decides what is prefetched: rows below
   //           max(rows_hint, 1) <= rows of experts below n, so every prefetched address lies
   //           inside x.
   {
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
       if constexpr (kSilu) prefetch_l2(src + p.hidden);
     };
     if constexpr (kMasked) {
-      if (p.rows_hint > 0u || !Tune::f16_silu) {
+      {
         const uint32_t rh = p.rows_hint > 0u ? p.rows_hint : 1u;
         const uint32_t rhm = p.rows_hint > 0u ? p.rows_hint_magic : 0xFFFFFFFFu;
         const uint32_t u = (first_task(Tune::round_robin) << (5u - lu_log2)) + (lane >> lu_log2);
@@ -189,6 +193,8 @@ __global__ void __launch_bounds__((Tuning<kFp16, kSilu, kMasked, kLight != 0>::t
       }
     }
   }
+
+  if constexpr (kSilu && !kCopyFirst) copy_to_smem_async<kT>(smem, kSiluF16, kSiluF16Words / 4);
 
   griddep_wait();
   griddep_launch_dependents();
